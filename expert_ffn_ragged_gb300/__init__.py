@@ -1,0 +1,213 @@
+"""Python binding of librd, the GB300 (sm_103a) ragged_dot library.
+
+Argument marshalling only: every step of the path runs in the CUDA kernels
+of ``librd.so`` behind the C ABI declared in ``include/rd.h``.  torch is used
+for device memory and the current stream, nothing else.  There is no CPU or
+library fallback: if the library is missing, every call raises.
+
+Functions (same names as the C ABI, without the ``rd_`` prefix):
+
+* ``ragged_dot(lhs, rhs, group_sizes, ...)``             -> out [m, n] (or [m, n/2] with GLU)
+* ``ragged_dot_trans_rhs(lhs, rhs, group_sizes, ...)``   -> out [m, k]
+* ``trans_ragged_dot(x, y, group_sizes, ...)``           -> out [g_local, k, n]
+* ``glu_fwd(fused, limit=None)``                         -> out [rows, f]
+* ``glu_bwd(fused, d_out, limit=None)``                  -> d_fused [rows, 2f]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+__all__ = [
+    "load", "lib_path", "ragged_dot", "ragged_dot_trans_rhs", "trans_ragged_dot",
+    "glu_fwd", "glu_bwd", "RdError", "EPI_NONE", "EPI_SILU_GLU",
+    "STATUS_NEG_SIZE", "STATUS_OVERFLOW", "STATUS_TIMEOUT", "MAX_GROUPS",
+]
+
+EPI_NONE = 0
+EPI_SILU_GLU = 1
+STATUS_NEG_SIZE = 1
+STATUS_OVERFLOW = 2
+STATUS_TIMEOUT = 4
+MAX_GROUPS = 1024
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "librd.so")
+_lib = None
+
+
+class RdError(RuntimeError):
+    """A non-OK rd_status returned by the library."""
+
+    def __init__(self, code: int, message: str):
+        super().__init__(message)
+        self.code = code
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load librd.so (built by ``expert_ffn_ragged_gb300.build.build()``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"librd.so is not built ({_LIB_PATH}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(_LIB_PATH)
+    vp, i64, i32, ip = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p
+    grouped = [vp, vp, vp, i64, i64, i64, ip, i32, i32, i32, ip]
+    lib.rd_ragged_dot.argtypes = grouped + [ctypes.c_int, ip, vp]
+    lib.rd_ragged_dot_trans_rhs.argtypes = grouped + [ip, vp]
+    lib.rd_trans_ragged_dot.argtypes = grouped + [ip, vp]
+    lib.rd_glu_fwd.argtypes = [vp, vp, i64, i64, ip, vp]
+    lib.rd_glu_bwd.argtypes = [vp, vp, vp, i64, i64, ip, vp]
+    for fn in (lib.rd_ragged_dot, lib.rd_ragged_dot_trans_rhs, lib.rd_trans_ragged_dot,
+               lib.rd_glu_fwd, lib.rd_glu_bwd):
+        fn.restype = ctypes.c_int
+    lib.rd_status_string.argtypes = [ctypes.c_int]
+    lib.rd_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        msg = _lib.rd_status_string(code).decode()
+        raise RdError(code, f"{what}: {msg}")
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _bf16_2d(t, name):
+    import torch
+
+    if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 2-D bf16 CUDA tensor")
+
+
+def _group_args(group_sizes, limit, status):
+    import torch
+
+    if group_sizes.dtype != torch.int32 or group_sizes.dim() != 1 or not group_sizes.is_cuda:
+        raise ValueError("group_sizes must be a 1-D int32 CUDA tensor")
+    for name, t in (("limit", limit), ("status", status)):
+        if t is not None and (t.dtype != torch.int32 or t.numel() != 1 or not t.is_cuda):
+            raise ValueError(f"{name} must be a one-element int32 CUDA tensor")
+
+
+def ragged_dot(lhs, rhs, group_sizes, group_offset: int = 0, limit=None, epilogue: int = EPI_NONE,
+               out=None, status=None, stream=None):
+    """Grouped forward out[i] = lhs[i] @ rhs[group(i) - group_offset] (see rd_ragged_dot)."""
+    import torch
+
+    lib = load()
+    _bf16_2d(lhs, "lhs")
+    _group_args(group_sizes, limit, status)
+    if rhs.dtype != torch.bfloat16 or rhs.dim() != 3 or not rhs.is_contiguous():
+        raise ValueError("rhs must be a contiguous [g_local, k, n] bf16 CUDA tensor")
+    m, k = lhs.shape
+    g_local, k2, n = rhs.shape
+    if k2 != k:
+        raise ValueError("lhs and rhs disagree on k")
+    n_out = n // 2 if epilogue == EPI_SILU_GLU else n
+    if out is None:
+        out = torch.empty((m, n_out), dtype=torch.bfloat16, device=lhs.device)
+    code = lib.rd_ragged_dot(_ptr(lhs), _ptr(rhs), _ptr(out), m, k, n, _ptr(group_sizes),
+                             group_sizes.numel(), group_offset, g_local, _ptr(limit),
+                             int(epilogue), _ptr(status), _stream(stream))
+    _check(code, "rd_ragged_dot")
+    return out
+
+
+def ragged_dot_trans_rhs(lhs, rhs, group_sizes, group_offset: int = 0, limit=None, out=None,
+                         status=None, stream=None):
+    """out[i] = lhs[i] @ rhs[group(i) - group_offset]^T; lhs [m, n], rhs [g_local, k, n]."""
+    import torch
+
+    lib = load()
+    _bf16_2d(lhs, "lhs")
+    _group_args(group_sizes, limit, status)
+    if rhs.dtype != torch.bfloat16 or rhs.dim() != 3 or not rhs.is_contiguous():
+        raise ValueError("rhs must be a contiguous [g_local, k, n] bf16 CUDA tensor")
+    m, n = lhs.shape
+    g_local, k, n2 = rhs.shape
+    if n2 != n:
+        raise ValueError("lhs and rhs disagree on n")
+    if out is None:
+        out = torch.empty((m, k), dtype=torch.bfloat16, device=lhs.device)
+    code = lib.rd_ragged_dot_trans_rhs(_ptr(lhs), _ptr(rhs), _ptr(out), m, k, n, _ptr(group_sizes),
+                                       group_sizes.numel(), group_offset, g_local, _ptr(limit),
+                                       _ptr(status), _stream(stream))
+    _check(code, "rd_ragged_dot_trans_rhs")
+    return out
+
+
+def trans_ragged_dot(x, y, group_sizes, group_offset: int = 0, g_local: Optional[int] = None,
+                     limit=None, out=None, status=None, stream=None):
+    """out[j] = x[rows_j]^T @ y[rows_j] for the local groups; x [m, k], y [m, n]."""
+    import torch
+
+    lib = load()
+    _bf16_2d(x, "x")
+    _bf16_2d(y, "y")
+    _group_args(group_sizes, limit, status)
+    m, k = x.shape
+    m2, n = y.shape
+    if m2 != m:
+        raise ValueError("x and y disagree on m")
+    if g_local is None:
+        g_local = group_sizes.numel() - group_offset
+    if out is None:
+        out = torch.empty((g_local, k, n), dtype=torch.bfloat16, device=x.device)
+    code = lib.rd_trans_ragged_dot(_ptr(x), _ptr(y), _ptr(out), m, k, n, _ptr(group_sizes),
+                                   group_sizes.numel(), group_offset, g_local, _ptr(limit),
+                                   _ptr(status), _stream(stream))
+    _check(code, "rd_trans_ragged_dot")
+    return out
+
+
+def glu_fwd(fused, limit=None, out=None, stream=None):
+    """silu(gate) * up over the rows below limit of a fused [rows, 2f] buffer."""
+    import torch
+
+    lib = load()
+    _bf16_2d(fused, "fused")
+    rows, w = fused.shape
+    f = w // 2
+    if out is None:
+        out = torch.empty((rows, f), dtype=torch.bfloat16, device=fused.device)
+    code = lib.rd_glu_fwd(_ptr(fused), _ptr(out), rows, f, _ptr(limit), _stream(stream))
+    _check(code, "rd_glu_fwd")
+    return out
+
+
+def glu_bwd(fused, d_out, limit=None, out=None, stream=None):
+    """[d_gate | d_up] for the rows below limit; fused [rows, 2f], d_out [rows, f]."""
+    import torch
+
+    lib = load()
+    _bf16_2d(fused, "fused")
+    _bf16_2d(d_out, "d_out")
+    rows, w = fused.shape
+    f = w // 2
+    if d_out.shape != (rows, f):
+        raise ValueError("d_out must be [rows, f]")
+    if out is None:
+        out = torch.empty((rows, 2 * f), dtype=torch.bfloat16, device=fused.device)
+    code = lib.rd_glu_bwd(_ptr(fused), _ptr(d_out), _ptr(out), rows, f, _ptr(limit),
+                          _stream(stream))
+    _check(code, "rd_glu_bwd")
+    return out

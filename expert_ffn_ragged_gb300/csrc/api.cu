@@ -1,0 +1,352 @@
+// api.cu -- the C ABI of librd (include/rd.h): argument checks, TMA tensor
+// maps, launch shapes.  Every check that can be made on the host is made
+// before any CUDA call, so bad arguments are rejected even without a GPU.
+// Nothing here synchronises, allocates or copies device data to the host.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/rd.h"
+#include "gemm_args.h"
+
+namespace rd {
+namespace {
+
+constexpr uint64_t kTimeoutNs = 4000000000ull;  // bound of any single wait inside a kernel
+constexpr int64_t kMaxDim = 0x7FFFFFFF;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// SM count of the current device, and whether it is an sm_103 part
+rd_status current_device(int* sms) {
+  static std::mutex mu;
+  static int cached_sms[64];
+  static int cached_state[64];  // 0 unknown, 1 supported, 2 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RD_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return RD_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached_state[dev] == 0) {
+    int major = 0, minor = 0, count = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return RD_ERR_CUDA;
+    cached_sms[dev] = count;
+    cached_state[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  *sms = cached_sms[dev];
+  return cached_state[dev] == 1 ? RD_OK : RD_ERR_UNSUPPORTED;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
+  if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// bf16 tensor map with 128-byte swizzle; dims/strides innermost first
+rd_status encode(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                 const uint64_t* strides_bytes, const uint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return RD_ERR_CUDA;
+  cuuint64_t gdim[5], gstride[4];
+  cuuint32_t gbox[5], estride[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    gbox[i] = box[i];
+    estride[i] = 1;
+  }
+  for (int i = 0; i < rank - 1; ++i) gstride[i] = strides_bytes[i];
+  const CUresult r =
+      fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim, gstride,
+         gbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? RD_OK : RD_ERR_UNSUPPORTED;
+}
+
+// checks shared by the three grouped calls
+rd_status check_groups(int64_t m, int64_t k, int64_t n, const int32_t* group_sizes,
+                       int32_t g_total, int32_t group_offset, int32_t g_local,
+                       const int32_t* limit, const int32_t* status) {
+  if (m < 0 || k < 0 || n < 0) return RD_ERR_INVALID_ARG;
+  if (group_sizes == nullptr) return RD_ERR_INVALID_ARG;
+  if (g_total < 1 || g_local < 1 || group_offset < 0 ||
+      static_cast<int64_t>(group_offset) + g_local > g_total)
+    return RD_ERR_INVALID_ARG;
+  if (g_total > RD_MAX_GROUPS) return RD_ERR_UNSUPPORTED;
+  if (m > kMaxDim || k > kMaxDim || n > kMaxDim) return RD_ERR_UNSUPPORTED;
+  if (k % 8 != 0 || n % 8 != 0) return RD_ERR_UNSUPPORTED;
+  const uintptr_t a4 = 3u;
+  if ((reinterpret_cast<uintptr_t>(group_sizes) & a4) || (reinterpret_cast<uintptr_t>(limit) & a4) ||
+      (reinterpret_cast<uintptr_t>(status) & a4))
+    return RD_ERR_UNSUPPORTED;
+  return RD_OK;
+}
+
+// the output must not overlap any input (or the control words)
+bool out_aliases(const void* out, uint64_t out_bytes, const void* in0, uint64_t b0,
+                 const void* in1, uint64_t b1, const void* gs, uint64_t bgs, const void* limit,
+                 const void* status) {
+  return overlap(out, out_bytes, in0, b0) || overlap(out, out_bytes, in1, b1) ||
+         overlap(out, out_bytes, gs, bgs) || overlap(out, out_bytes, limit, 4) ||
+         overlap(out, out_bytes, status, 4);
+}
+
+int grid_for(int sms, int64_t tiles_upper_bound) {
+  int64_t g = tiles_upper_bound < 1 ? 1 : tiles_upper_bound;
+  return static_cast<int>(g < sms ? g : sms);
+}
+
+}  // namespace
+}  // namespace rd
+
+using namespace rd;
+
+extern "C" rd_status rd_ragged_dot(const void* lhs, const void* rhs, void* out, int64_t m,
+                                   int64_t k, int64_t n, const int32_t* group_sizes,
+                                   int32_t g_total, int32_t group_offset, int32_t g_local,
+                                   const int32_t* limit, rd_epilogue epi, int32_t* status,
+                                   rd_stream_t stream) {
+  const bool glu = epi == RD_EPI_SILU_GLU;
+  if (epi != RD_EPI_NONE && !glu) return RD_ERR_INVALID_ARG;
+  rd_status st = check_groups(m, k, n, group_sizes, g_total, group_offset, g_local, limit, status);
+  if (st != RD_OK) return st;
+  if (glu && n % 16 != 0) return n % 2 ? RD_ERR_INVALID_ARG : RD_ERR_UNSUPPORTED;
+  const int64_t n_out = glu ? n / 2 : n;
+  if ((m > 0 && k > 0 && lhs == nullptr) || (k > 0 && n > 0 && rhs == nullptr) ||
+      (m > 0 && n_out > 0 && out == nullptr))
+    return RD_ERR_INVALID_ARG;
+  if (!aligned16(lhs) || !aligned16(rhs) || !aligned16(out)) return RD_ERR_UNSUPPORTED;
+  const uint64_t out_bytes = static_cast<uint64_t>(m) * n_out * 2;
+  if (out_aliases(out, out_bytes, lhs, static_cast<uint64_t>(m) * k * 2, rhs,
+                  static_cast<uint64_t>(g_local) * k * n * 2, group_sizes,
+                  static_cast<uint64_t>(g_total) * 4, limit, status))
+    return RD_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = current_device(&sms)) != RD_OK) return st;
+  if (m == 0 || n_out == 0) return RD_OK;
+
+  CUtensorMap ta = {}, tb = {};
+  if (k > 0) {
+    const uint64_t da[2] = {static_cast<uint64_t>(k), static_cast<uint64_t>(m)};
+    const uint64_t sa[1] = {static_cast<uint64_t>(k) * 2};
+    const uint32_t ba[2] = {64, kBM};
+    if ((st = encode(&ta, lhs, 2, da, sa, ba)) != RD_OK) return st;
+    const uint64_t db[3] = {static_cast<uint64_t>(n), static_cast<uint64_t>(k),
+                            static_cast<uint64_t>(g_local)};
+    const uint64_t sb[2] = {static_cast<uint64_t>(n) * 2, static_cast<uint64_t>(k) * n * 2};
+    const uint32_t bb[3] = {64, kBK, 1};
+    if ((st = encode(&tb, rhs, 3, db, sb, bb)) != RD_OK) return st;
+  }
+  GemmArgs a = {};
+  a.group_sizes = group_sizes;
+  a.limit = limit;
+  a.status = status;
+  a.out = out;
+  a.m = static_cast<int32_t>(m);
+  a.kc = static_cast<int32_t>(k);
+  a.n_out = static_cast<int32_t>(n_out);
+  a.m_out = 0;
+  a.g_total = g_total;
+  a.group_offset = group_offset;
+  a.g_local = g_local;
+  a.glu_f = static_cast<int32_t>(n_out);
+  const int tile_w = glu ? kBN / 2 : kBN;
+  a.n_tiles = static_cast<int32_t>((n_out + tile_w - 1) / tile_w);
+  a.dw_m_tiles = 0;
+  a.timeout_ns = kTimeoutNs;
+  const int grid = grid_for(sms, ((m + kBM - 1) / kBM + g_local) * a.n_tiles);
+  return launch_gemm_fwd(glu, ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? RD_OK
+             : RD_ERR_CUDA;
+}
+
+extern "C" rd_status rd_ragged_dot_trans_rhs(const void* lhs, const void* rhs, void* out,
+                                             int64_t m, int64_t k, int64_t n,
+                                             const int32_t* group_sizes, int32_t g_total,
+                                             int32_t group_offset, int32_t g_local,
+                                             const int32_t* limit, int32_t* status,
+                                             rd_stream_t stream) {
+  rd_status st = check_groups(m, k, n, group_sizes, g_total, group_offset, g_local, limit, status);
+  if (st != RD_OK) return st;
+  if ((m > 0 && n > 0 && lhs == nullptr) || (k > 0 && n > 0 && rhs == nullptr) ||
+      (m > 0 && k > 0 && out == nullptr))
+    return RD_ERR_INVALID_ARG;
+  if (!aligned16(lhs) || !aligned16(rhs) || !aligned16(out)) return RD_ERR_UNSUPPORTED;
+  if (out_aliases(out, static_cast<uint64_t>(m) * k * 2, lhs, static_cast<uint64_t>(m) * n * 2,
+                  rhs, static_cast<uint64_t>(g_local) * k * n * 2, group_sizes,
+                  static_cast<uint64_t>(g_total) * 4, limit, status))
+    return RD_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = current_device(&sms)) != RD_OK) return st;
+  if (m == 0 || k == 0) return RD_OK;
+
+  CUtensorMap ta = {}, tb = {};
+  if (n > 0) {
+    const uint64_t da[2] = {static_cast<uint64_t>(n), static_cast<uint64_t>(m)};
+    const uint64_t sa[1] = {static_cast<uint64_t>(n) * 2};
+    const uint32_t ba[2] = {64, kBM};
+    if ((st = encode(&ta, lhs, 2, da, sa, ba)) != RD_OK) return st;
+    const uint64_t db[3] = {static_cast<uint64_t>(n), static_cast<uint64_t>(k),
+                            static_cast<uint64_t>(g_local)};
+    const uint64_t sb[2] = {static_cast<uint64_t>(n) * 2, static_cast<uint64_t>(k) * n * 2};
+    const uint32_t bb[3] = {64, kBN, 1};
+    if ((st = encode(&tb, rhs, 3, db, sb, bb)) != RD_OK) return st;
+  }
+  GemmArgs a = {};
+  a.group_sizes = group_sizes;
+  a.limit = limit;
+  a.status = status;
+  a.out = out;
+  a.m = static_cast<int32_t>(m);
+  a.kc = static_cast<int32_t>(n);
+  a.n_out = static_cast<int32_t>(k);
+  a.g_total = g_total;
+  a.group_offset = group_offset;
+  a.g_local = g_local;
+  a.n_tiles = static_cast<int32_t>((k + kBN - 1) / kBN);
+  a.timeout_ns = kTimeoutNs;
+  const int grid = grid_for(sms, ((m + kBM - 1) / kBM + g_local) * a.n_tiles);
+  return launch_gemm_dx(ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RD_OK
+             : RD_ERR_CUDA;
+}
+
+extern "C" rd_status rd_trans_ragged_dot(const void* x, const void* y, void* out, int64_t m,
+                                         int64_t k, int64_t n, const int32_t* group_sizes,
+                                         int32_t g_total, int32_t group_offset, int32_t g_local,
+                                         const int32_t* limit, int32_t* status,
+                                         rd_stream_t stream) {
+  rd_status st = check_groups(m, k, n, group_sizes, g_total, group_offset, g_local, limit, status);
+  if (st != RD_OK) return st;
+  if ((m > 0 && k > 0 && x == nullptr) || (m > 0 && n > 0 && y == nullptr) ||
+      (k > 0 && n > 0 && out == nullptr))
+    return RD_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(out)) return RD_ERR_UNSUPPORTED;
+  if (out_aliases(out, static_cast<uint64_t>(g_local) * k * n * 2, x,
+                  static_cast<uint64_t>(m) * k * 2, y, static_cast<uint64_t>(m) * n * 2,
+                  group_sizes, static_cast<uint64_t>(g_total) * 4, limit, status))
+    return RD_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = current_device(&sms)) != RD_OK) return st;
+  if (k == 0 || n == 0) return RD_OK;
+
+  CUtensorMap ta = {}, tb = {};
+  if (m > 0) {
+    const uint64_t da[2] = {static_cast<uint64_t>(k), static_cast<uint64_t>(m)};
+    const uint64_t sa[1] = {static_cast<uint64_t>(k) * 2};
+    const uint32_t ba[2] = {64, kBK};
+    if ((st = encode(&ta, x, 2, da, sa, ba)) != RD_OK) return st;
+    const uint64_t db[2] = {static_cast<uint64_t>(n), static_cast<uint64_t>(m)};
+    const uint64_t sb[1] = {static_cast<uint64_t>(n) * 2};
+    const uint32_t bb[2] = {64, kBK};
+    if ((st = encode(&tb, y, 2, db, sb, bb)) != RD_OK) return st;
+  }
+  GemmArgs a = {};
+  a.group_sizes = group_sizes;
+  a.limit = limit;
+  a.status = status;
+  a.out = out;
+  a.m = static_cast<int32_t>(m);
+  a.kc = static_cast<int32_t>(m);
+  a.n_out = static_cast<int32_t>(n);
+  a.m_out = static_cast<int32_t>(k);
+  a.g_total = g_total;
+  a.group_offset = group_offset;
+  a.g_local = g_local;
+  a.n_tiles = static_cast<int32_t>((n + kBN - 1) / kBN);
+  a.dw_m_tiles = static_cast<int32_t>((k + kBM - 1) / kBM);
+  a.timeout_ns = kTimeoutNs;
+  const int64_t tiles = static_cast<int64_t>(g_local) * a.dw_m_tiles * a.n_tiles;
+  if (tiles > kMaxDim) return RD_ERR_UNSUPPORTED;
+  const int grid = grid_for(sms, tiles);
+  return launch_gemm_dw(ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RD_OK
+             : RD_ERR_CUDA;
+}
+
+namespace {
+rd_status check_glu(const void* a, const void* b, const void* out, int64_t rows, int64_t f,
+                    const int32_t* limit) {
+  if (rows < 0 || f < 0) return RD_ERR_INVALID_ARG;
+  if (rows > kMaxDim || f > kMaxDim / 2) return RD_ERR_UNSUPPORTED;
+  if (f % 8 != 0) return RD_ERR_UNSUPPORTED;
+  if (rows > 0 && f > 0 && (a == nullptr || b == nullptr || out == nullptr))
+    return RD_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(b) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(limit) & 3u))
+    return RD_ERR_UNSUPPORTED;
+  return RD_OK;
+}
+}  // namespace
+
+extern "C" rd_status rd_glu_fwd(const void* fused, void* out, int64_t rows, int64_t f,
+                                const int32_t* limit, rd_stream_t stream) {
+  rd_status st = check_glu(fused, fused, out, rows, f, limit);
+  if (st != RD_OK) return st;
+  if (overlap(out, static_cast<uint64_t>(rows) * f * 2, fused,
+              static_cast<uint64_t>(rows) * f * 4) ||
+      overlap(out, static_cast<uint64_t>(rows) * f * 2, limit, 4))
+    return RD_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = current_device(&sms)) != RD_OK) return st;
+  if (rows == 0 || f == 0) return RD_OK;
+  const int grid = grid_for(sms * 8, (rows + 7) / 8);
+  return launch_glu_fwd(fused, out, static_cast<int32_t>(rows), static_cast<int32_t>(f), limit,
+                        grid, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RD_OK
+             : RD_ERR_CUDA;
+}
+
+extern "C" rd_status rd_glu_bwd(const void* fused, const void* d_out, void* d_fused, int64_t rows,
+                                int64_t f, const int32_t* limit, rd_stream_t stream) {
+  rd_status st = check_glu(fused, d_out, d_fused, rows, f, limit);
+  if (st != RD_OK) return st;
+  const uint64_t ob = static_cast<uint64_t>(rows) * f * 4;
+  if (overlap(d_fused, ob, fused, ob) ||
+      overlap(d_fused, ob, d_out, static_cast<uint64_t>(rows) * f * 2) ||
+      overlap(d_fused, ob, limit, 4))
+    return RD_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = current_device(&sms)) != RD_OK) return st;
+  if (rows == 0 || f == 0) return RD_OK;
+  const int grid = grid_for(sms * 8, (rows + 7) / 8);
+  return launch_glu_bwd(fused, d_out, d_fused, static_cast<int32_t>(rows),
+                        static_cast<int32_t>(f), limit, grid,
+                        reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RD_OK
+             : RD_ERR_CUDA;
+}
+
+extern "C" const char* rd_status_string(rd_status s) {
+  switch (s) {
+    case RD_OK: return "RD_OK";
+    case RD_ERR_INVALID_ARG: return "RD_ERR_INVALID_ARG: invalid argument";
+    case RD_ERR_UNSUPPORTED: return "RD_ERR_UNSUPPORTED: unsupported shape, alignment or device";
+    case RD_ERR_CUDA: return "RD_ERR_CUDA: CUDA runtime error";
+  }
+  return "unknown rd_status";
+}

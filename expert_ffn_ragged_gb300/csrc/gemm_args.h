@@ -1,0 +1,62 @@
+// gemm_args.h -- launch arguments of the grouped-GEMM kernels (host and
+// device), the tile shape, and the host-side launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rd {
+
+enum GemmOp : int {
+  kOpFwd = 0,  // out[i] = lhs[i] @ rhs[j]             (A K-major, B MN-major)
+  kOpDx = 1,   // out[i] = lhs[i] @ rhs[j]^T           (A K-major, B K-major)
+  kOpDw = 2    // out[j] = x[rows_j]^T @ y[rows_j]     (A MN-major, B MN-major)
+};
+
+// UMMA tile: 128 x 256 f32 accumulator per tile, 64-deep K blocks (one
+// 128-byte swizzle atom of bf16), 4-stage shared-memory ring.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warps 6-7 zero fill
+constexpr int kStageBytesA = kBM * kBK * 2;
+constexpr int kStageBytesB = kBN * kBK * 2;
+constexpr int kTmemCols = 2 * kBN;  // two accumulators (double buffer)
+constexpr int kMaxGroups = 1024;
+
+struct GemmArgs {
+  const int32_t* group_sizes;  // [g_total], device
+  const int32_t* limit;        // device scalar or null
+  int32_t* status;             // device or null
+  void* out;                   // bf16 output
+  int32_t m;                   // token rows
+  int32_t kc;                  // contraction length (fwd: k, dx: n); dw: unused (rows of each group)
+  int32_t n_out;               // output width (columns stored)
+  int32_t m_out;               // dw: rows of each weight block (= k)
+  int32_t g_total;
+  int32_t group_offset;
+  int32_t g_local;
+  int32_t glu_f;               // fwd with GLU: first column of the up half in rhs (= n / 2)
+  int32_t n_tiles;             // output column tiles
+  int32_t dw_m_tiles;          // dw: 128-row tiles of each weight block
+  uint64_t timeout_ns;         // bound of every wait inside the kernel
+};
+
+// shared memory the grouped-GEMM kernel needs (ring + bookkeeping + alignment slack)
+size_t gemm_smem_bytes();
+
+cudaError_t launch_gemm_fwd(bool glu, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                            const GemmArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_dx(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                           const GemmArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_dw(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                           const GemmArgs& args, int grid, cudaStream_t stream);
+
+cudaError_t launch_glu_fwd(const void* fused, void* out, int32_t rows, int32_t f,
+                           const int32_t* limit, int grid, cudaStream_t stream);
+cudaError_t launch_glu_bwd(const void* fused, const void* d_out, void* d_fused, int32_t rows,
+                           int32_t f, const int32_t* limit, int grid, cudaStream_t stream);
+
+}  // namespace rd

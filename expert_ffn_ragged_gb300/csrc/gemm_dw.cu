@@ -1,0 +1,10 @@
+// gemm_dw.cu -- the trans_ragged_dot grouped GEMM (per-group weight gradient).
+#include "gemm_kernel.cuh"
+
+namespace rd {
+cudaError_t launch_gemm_dw(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
+                           int grid, cudaStream_t s) {
+  return launch_gemm_impl<kOpDw, false>(a, b, args, grid, s);
+}
+size_t gemm_smem_bytes() { return kGemmSmemBytes; }
+}  // namespace rd

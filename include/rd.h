@@ -1,0 +1,167 @@
+/*
+ * rd.h -- C ABI of librd: the MoE ragged_dot (grouped GEMM) hot path on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Every entry point takes plain device pointers and sizes, enqueues work on
+ * the caller's CUDA stream and returns at once.  The library never
+ * synchronises, never copies device data to the host and allocates nothing
+ * per call; group_sizes and limit stay on the device and are read by the
+ * kernels themselves.  A call can therefore be captured in a CUDA graph,
+ * and replays follow device-side changes to group_sizes and limit.  The
+ * first call of each entry point in a process sets a kernel attribute
+ * (dynamic shared memory size); make it before a stream capture begins.
+ *
+ * Layout: every matrix is row-major and contiguous, bf16 unless stated.
+ * Ownership: the caller owns every buffer; the library keeps no pointer
+ * after the call returns (the work it enqueued still reads and writes the
+ * buffers until it completes on the stream).
+ *
+ * Group semantics (all grouped calls):
+ *   L      = min(max(*limit, 0), m), or m when limit is NULL.
+ *   s[i]   = min(sum_{j<i} max(group_sizes[j], 0), L), i = 0..g_total.
+ *   Group i owns rows [s[i], s[i+1]).  Local group j (0 <= j < g_local) is
+ *   global group group_offset + j and uses rhs / weight block j.
+ *   Rows in [0, L) outside the local groups are written as +0; rows >= L of
+ *   every output are never written and rows >= L of every input are never
+ *   read.
+ *
+ * Errors: invalid arguments are rejected before anything is enqueued
+ * (RD_ERR_INVALID_ARG / RD_ERR_UNSUPPORTED); a failed launch returns
+ * RD_ERR_CUDA.  Bad data found on the device (a negative group size, sizes
+ * summing past m, a bounded wait that ran out) never traps: the kernel
+ * clamps and, when `status` is not NULL, ORs an RD_STATUS_* bit into
+ * *status.  The library never clears *status.
+ */
+#ifndef RD_H_
+#define RD_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* rd_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  RD_OK = 0,
+  RD_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad group range, aliasing */
+  RD_ERR_UNSUPPORTED = 2, /* width not a multiple of 8, misaligned pointer, too many groups, not sm_103 */
+  RD_ERR_CUDA = 3         /* the CUDA runtime reported an error at launch */
+} rd_status;
+
+typedef enum {
+  RD_EPI_NONE = 0,    /* store the f32 accumulator rounded to bf16 */
+  RD_EPI_SILU_GLU = 1 /* out[:, c] = bf16(silu(acc[:, c]) * acc[:, F + c]), F = n / 2 */
+} rd_epilogue;
+
+/* device status bits, ORed into *status */
+#define RD_STATUS_NEG_SIZE 1 /* a group size < 0 was taken as 0 */
+#define RD_STATUS_OVERFLOW 2 /* the group sizes sum past m; boundaries clamped */
+#define RD_STATUS_TIMEOUT 4  /* a bounded wait inside a kernel ran out; outputs incomplete */
+
+/* largest g_total accepted by the grouped calls */
+#define RD_MAX_GROUPS 1024
+
+/*
+ * rd_ragged_dot -- grouped forward.
+ *   out[i, :] = lhs[i, :] @ rhs[j, :, :] for every row i of local group j.
+ * Defined by SkyRL PR #867 "Integrate ragged_dot pallas kernel with
+ * group_offset support" (the suggested fast_ragged_dot body: group
+ * boundaries from a cumulative sum with an initial zero, only the local
+ * groups computed, rows outside them zeroed) and MaxText PR #5760 "MoE wo
+ * FSDP sharding and valid-rows-only MoE kernels" (commit message: only rows
+ * [0, limit) of the packed buffer are valid; the SiLU-GLU over the fused
+ * [gate | up] buffer, computed in f32 and rounded only at the output).
+ *
+ *   lhs          [m, k] bf16, device
+ *   rhs          [g_local, k, n] bf16, device
+ *   out          [m, n] bf16 (epi = NONE) or [m, n/2] (epi = SILU_GLU), device
+ *   group_sizes  [g_total] int32, device
+ *   group_offset first local group (host int), 0 <= group_offset,
+ *                group_offset + g_local <= g_total <= RD_MAX_GROUPS
+ *   limit        device int32 scalar or NULL
+ *   epi          RD_EPI_NONE or RD_EPI_SILU_GLU (gate = columns [0, n/2) of
+ *                the product, up = columns [n/2, n))
+ *   status       device int32 or NULL
+ * Accumulation is f32; the bf16 store rounds to nearest even.
+ * Requires k % 8 == 0, n % 8 == 0 (n/2 % 8 == 0 with the GLU) and 16-byte
+ * aligned pointers; out must not overlap lhs, rhs or group_sizes.
+ */
+rd_status rd_ragged_dot(const void* lhs, const void* rhs, void* out, int64_t m, int64_t k,
+                        int64_t n, const int32_t* group_sizes, int32_t g_total,
+                        int32_t group_offset, int32_t g_local, const int32_t* limit,
+                        rd_epilogue epi, int32_t* status, rd_stream_t stream);
+
+/*
+ * rd_ragged_dot_trans_rhs -- the trans_rhs form (input gradient dx).
+ *   out[i, :] = lhs[i, :] @ rhs[j, :, :]^T for every row i of local group j.
+ * Defined by SkyRL PR #867 (review comment on the trans_ragged_dot
+ * backward: dx = ragged_dot(y, do, group_sizes, trans_rhs=True)).
+ *
+ *   lhs  [m, n] bf16 (the output gradient), rhs [g_local, k, n] bf16,
+ *   out  [m, k] bf16.  Other arguments as rd_ragged_dot.
+ * Requires k % 8 == 0, n % 8 == 0, 16-byte aligned pointers, no overlap.
+ */
+rd_status rd_ragged_dot_trans_rhs(const void* lhs, const void* rhs, void* out, int64_t m,
+                                  int64_t k, int64_t n, const int32_t* group_sizes,
+                                  int32_t g_total, int32_t group_offset, int32_t g_local,
+                                  const int32_t* limit, int32_t* status, rd_stream_t stream);
+
+/*
+ * rd_trans_ragged_dot -- per-group weight gradient.
+ *   out[j, :, :] = x[rows_j, :]^T @ y[rows_j, :] for each local group j;
+ *   a group without rows (or whose rows all lie at or past L) gives zeros.
+ * Defined by SkyRL PR #867 (_gpu_trans_ragged_dot_fwd: x [m, k], y [m, n],
+ * f32 accumulation) and MaxText PR #5760 (commit message: the grouped
+ * matmuls skip rows outside the groups and past limit).
+ *
+ *   x [m, k] bf16, y [m, n] bf16, out [g_local, k, n] bf16 (f32 accumulated).
+ *   Other arguments as rd_ragged_dot.
+ * Requires k % 8 == 0, n % 8 == 0, 16-byte aligned pointers, no overlap.
+ */
+rd_status rd_trans_ragged_dot(const void* x, const void* y, void* out, int64_t m, int64_t k,
+                              int64_t n, const int32_t* group_sizes, int32_t g_total,
+                              int32_t group_offset, int32_t g_local, const int32_t* limit,
+                              int32_t* status, rd_stream_t stream);
+
+/*
+ * rd_glu_fwd -- SiLU-GLU forward over the valid rows of a fused buffer.
+ *   out[r, c] = bf16( g / (1 + exp(-g)) * u ),  g = fused[r, c], u = fused[r, f + c],
+ *   for r < L; rows >= L of out are not written and of fused not read.
+ * Defined by MaxText PR #5760 (commit message, kernels/ragged/glu_rows.py:
+ * gate and up read in place from the fused buffer, XLA's op sequence
+ * negate, exp, +1, divide, multiply in f32, rounded only at the output).
+ *
+ *   fused [rows, 2f] bf16, out [rows, f] bf16, limit device int32 or NULL.
+ * Requires f % 8 == 0, 16-byte aligned pointers, out not overlapping fused.
+ */
+rd_status rd_glu_fwd(const void* fused, void* out, int64_t rows, int64_t f,
+                     const int32_t* limit, rd_stream_t stream);
+
+/*
+ * rd_glu_bwd -- SiLU-GLU backward, writing [d_gate | d_up] in one pass.
+ *   with g, u as above and d = d_out[r, c], in f32:
+ *   e = exp(-g), den = 1 + e, sig = 1 / den, silu = g / den,
+ *   d_fused[r, f + c] = bf16(d * silu),
+ *   d_fused[r, c]     = bf16((d * u) * (sig * (1 + g * (1 - sig)))),
+ *   and any result that rounds to -0 is stored as +0; rows r < L only.
+ * Defined by MaxText PR #5760 (commit message: the backward writes
+ * [d_gate | d_up] in one pass with the -0 -> +0 fix, recomputing the
+ * forward from the saved fused buffer).
+ *
+ *   fused [rows, 2f] bf16, d_out [rows, f] bf16, d_fused [rows, 2f] bf16.
+ * Requires f % 8 == 0, 16-byte aligned pointers, d_fused not overlapping
+ * the inputs.
+ */
+rd_status rd_glu_bwd(const void* fused, const void* d_out, void* d_fused, int64_t rows,
+                     int64_t f, const int32_t* limit, rd_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char* rd_status_string(rd_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RD_H_ */

@@ -1,0 +1,296 @@
+"""GPU parity of the grouped GEMMs against the float64 oracle, through the C ABI.
+
+Small shapes that span several 128x256 tiles and ragged edges in every
+dimension: group sizes 0, 1, BM-1, BM, BM+1, k and n not multiples of the
+tile, group offsets, valid-row limits, NaN-poisoned input rows past the
+limit, sentinel-filled output rows past the limit and canary rows after the
+output buffer.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import bf16 as obf
+from parity_util import assert_close, gemm_tol, glu_epilogue_tol
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+SENT = 0x3C3C          # sentinel bf16 pattern for rows that must stay untouched
+CANARY_ROWS = 4
+EDGE_SIZES = [0, 1, 127, 128, 129, 0, 255, 3]   # sum 643
+
+
+def _normal(rng, shape, var=1.0):
+    from workloads import normal_bf16_np
+    return normal_bf16_np(rng, shape, var)
+
+
+def _i32(vals):
+    return torch.tensor(vals, dtype=torch.int32, device=DEV)
+
+
+def _sentinel_buffer(rows, cols, lead=()):
+    buf = torch.empty(lead + (rows + CANARY_ROWS, cols), dtype=torch.bfloat16, device=DEV)
+    buf.view(torch.int16).fill_(SENT)
+    return buf
+
+
+def _f64(t):
+    return obf.torch_bf16_to_f64(t)
+
+
+def _check_rows(bits, m, L, local_mask):
+    """rows >= L and canaries keep the sentinel; rows < L outside the groups are +0."""
+    assert np.all(bits[L:] == SENT), "a row at or past the limit (or a canary row) was written"
+    zero_rows = ~local_mask[:m]
+    zero_rows[L:] = False
+    assert np.all(bits[:m][zero_rows] == 0), "rows outside the local groups are not +0"
+
+
+def run_fwd(rd, m, k, n, sizes, off=0, gl=None, limit=None, glu=False, seed=0, poison=True):
+    rng = np.random.default_rng(seed)
+    g_total = len(sizes)
+    gl = g_total - off if gl is None else gl
+    lhs = _normal(rng, (m, k))
+    rhs = _normal(rng, (gl, k, n), 1.0 / max(k, 1))
+    b, L = oracle.group_bounds(sizes, m, limit)
+    lhs_dev = lhs.clone()
+    if poison:
+        lhs_dev[L:] = float("nan")
+    n_out = n // 2 if glu else n
+    buf = _sentinel_buffer(m, n_out)
+    status = _i32([0])
+    rd.ragged_dot(lhs_dev.to(DEV), rhs.to(DEV), _i32(sizes), group_offset=off,
+                  limit=None if limit is None else _i32([limit]),
+                  epilogue=rd.EPI_SILU_GLU if glu else rd.EPI_NONE, out=buf[:m], status=status)
+    torch.cuda.synchronize()
+    bits = obf.torch_bf16_bits(buf)
+    got = _f64(buf[:m])
+    a64, w64 = _f64(lhs), _f64(rhs)
+    local = np.zeros(m, bool)
+    local[b[off]:b[off + gl]] = True
+    _check_rows(bits, m, L, local)
+    amax = np.abs(a64[:L]).max() if L else 0.0
+    bmax = np.abs(w64).max() if w64.size else 0.0
+    if glu:
+        plain = oracle.ragged_dot(a64, w64, sizes, off, limit)
+        F = n_out
+        E = 1e-3 * math.sqrt(max(k, 1)) * amax * bmax
+        ref, tol = glu_epilogue_tol(plain[:, :F], plain[:, F:], E)
+        ref_o = oracle.ragged_dot(a64, w64, sizes, off, limit, glu=True)
+        np.testing.assert_allclose(ref[local], ref_o[local], rtol=1e-12, atol=1e-300)
+    else:
+        ref = oracle.ragged_dot(a64, w64, sizes, off, limit)
+        tol = gemm_tol(ref, k, amax, bmax)
+    assert_close(got[local], ref[local], tol[local], "forward")
+    assert int(status.item()) == 0
+    return got
+
+
+def run_dx(rd, m, k, n, sizes, off=0, gl=None, limit=None, seed=0):
+    rng = np.random.default_rng(seed)
+    gl = len(sizes) - off if gl is None else gl
+    do = _normal(rng, (m, n))
+    w = _normal(rng, (gl, k, n), 1.0 / max(k, 1))
+    b, L = oracle.group_bounds(sizes, m, limit)
+    do_dev = do.clone()
+    do_dev[L:] = float("nan")
+    buf = _sentinel_buffer(m, k)
+    rd.ragged_dot_trans_rhs(do_dev.to(DEV), w.to(DEV), _i32(sizes), group_offset=off,
+                            limit=None if limit is None else _i32([limit]), out=buf[:m])
+    torch.cuda.synchronize()
+    bits = obf.torch_bf16_bits(buf)
+    got = _f64(buf[:m])
+    a64, w64 = _f64(do), _f64(w)
+    local = np.zeros(m, bool)
+    local[b[off]:b[off + gl]] = True
+    _check_rows(bits, m, L, local)
+    ref = oracle.ragged_dot_trans_rhs(a64, w64, sizes, off, limit)
+    amax = np.abs(a64[:L]).max() if L else 0.0
+    tol = gemm_tol(ref, n, amax, np.abs(w64).max())
+    assert_close(got[local], ref[local], tol[local], "dx")
+
+
+def run_dw(rd, m, k, n, sizes, off=0, gl=None, limit=None, seed=0):
+    rng = np.random.default_rng(seed)
+    gl = len(sizes) - off if gl is None else gl
+    x = _normal(rng, (m, k))
+    y = _normal(rng, (m, n))
+    b, L = oracle.group_bounds(sizes, m, limit)
+    x_dev, y_dev = x.clone(), y.clone()
+    # rows past the limit and rows outside the local groups must not enter any sum
+    x_dev[L:] = float("nan")
+    y_dev[L:] = float("nan")
+    if b[off] > 0:
+        x_dev[: b[off]] = float("nan")
+        y_dev[: b[off]] = float("nan")
+    out = torch.empty((gl, k, n), dtype=torch.bfloat16, device=DEV)
+    out.view(torch.int16).fill_(SENT)
+    rd.trans_ragged_dot(x_dev.to(DEV), y_dev.to(DEV), _i32(sizes), group_offset=off, g_local=gl,
+                        limit=None if limit is None else _i32([limit]), out=out)
+    torch.cuda.synchronize()
+    got = _f64(out)
+    x64, y64 = _f64(x), _f64(y)
+    ref = oracle.trans_ragged_dot(x64, y64, sizes, off, gl, limit)
+    for j in range(gl):
+        cnt = int(b[off + j + 1] - b[off + j])
+        if cnt == 0:
+            assert np.all(obf.torch_bf16_bits(out[j]) == 0), f"empty group {j} not +0"
+            continue
+        rows = slice(b[off + j], b[off + j + 1])
+        tol = gemm_tol(ref[j], cnt, np.abs(x64[rows]).max(), np.abs(y64[rows]).max())
+        assert_close(got[j], ref[j], tol, f"dw group {j} ({cnt} rows)")
+
+
+# ------------------------------------------------------------------ forward
+def test_tiny_workload(rd_lib):
+    from workloads import tiny_fwd
+    w = tiny_fwd()
+    run_fwd(rd_lib, w.m, w.k, w.n, w.group_sizes.tolist(), seed=w.seed)
+
+
+@pytest.mark.parametrize("m,k,n", [(700, 136, 264), (700, 64, 512), (643, 520, 256)])
+def test_forward_ragged_edges(rd_lib, m, k, n):
+    run_fwd(rd_lib, m, k, n, EDGE_SIZES, seed=m + k + n)
+
+
+@pytest.mark.parametrize("off,gl,limit", [(2, 4, None), (2, 4, 500), (0, 8, 300), (7, 1, None),
+                                          (4, 3, 640)])
+def test_forward_offset_and_limit(rd_lib, off, gl, limit):
+    run_fwd(rd_lib, 700, 136, 264, EDGE_SIZES, off=off, gl=gl, limit=limit, seed=off * 7 + gl)
+
+
+@pytest.mark.parametrize("limit", [0, 1, 127, 128, 699, 700, 900])
+def test_forward_limit_sweep(rd_lib, limit):
+    run_fwd(rd_lib, 700, 72, 256, EDGE_SIZES, limit=limit, seed=limit)
+
+
+def test_forward_many_groups(rd_lib):
+    rng = np.random.default_rng(3)
+    sizes = rng.multinomial(1900, np.full(17, 1 / 17)).tolist()
+    run_fwd(rd_lib, 2048, 256, 512, sizes, off=3, gl=9, limit=1700, seed=3)
+
+
+@pytest.mark.parametrize("m,k,n,sizes", [(5, 64, 256, [5]), (1, 8, 8, [1]), (130, 8, 24, [64, 66]),
+                                         (300, 64, 256, [300])])
+def test_forward_small_and_single_group(rd_lib, m, k, n, sizes):
+    run_fwd(rd_lib, m, k, n, sizes, seed=m)
+
+
+@pytest.mark.parametrize("m,k,F,off,gl,limit", [(700, 136, 136, 0, 8, 650), (700, 64, 128, 2, 4, None),
+                                                (300, 256, 256, 0, 1, None), (700, 64, 8, 1, 5, 600)])
+def test_forward_glu_epilogue(rd_lib, m, k, F, off, gl, limit):
+    sizes = EDGE_SIZES if gl > 1 else [300]
+    run_fwd(rd_lib, m, k, 2 * F, sizes, off=off, gl=gl, limit=limit, glu=True, seed=F + off)
+
+
+def test_forward_k_zero_writes_zeros(rd_lib):
+    m, n = 300, 256
+    buf = _sentinel_buffer(m, n)
+    rd_lib.ragged_dot(torch.empty((m, 0), dtype=torch.bfloat16, device=DEV),
+                      torch.empty((2, 0, n), dtype=torch.bfloat16, device=DEV),
+                      _i32([100, 150]), out=buf[:m], limit=_i32([280]))
+    torch.cuda.synchronize()
+    bits = obf.torch_bf16_bits(buf)
+    assert np.all(bits[:280] == 0) and np.all(bits[280:] == SENT)
+
+
+def test_status_bits(rd_lib):
+    m, k, n = 256, 64, 256
+    lhs = torch.randn(m, k, device=DEV).to(torch.bfloat16)
+    rhs = torch.randn(3, k, n, device=DEV).to(torch.bfloat16)
+    status = _i32([0])
+    rd_lib.ragged_dot(lhs, rhs, _i32([100, -5, 200]), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == (rd_lib.STATUS_NEG_SIZE | rd_lib.STATUS_OVERFLOW)
+
+
+# ------------------------------------------------------------------ dx
+@pytest.mark.parametrize("m,k,n,off,gl,limit", [(700, 264, 136, 0, 8, None), (700, 264, 136, 2, 4, 500),
+                                                (643, 512, 72, 0, 8, 600), (700, 256, 520, 5, 3, None)])
+def test_dx(rd_lib, m, k, n, off, gl, limit):
+    run_dx(rd_lib, m, k, n, EDGE_SIZES, off=off, gl=gl, limit=limit, seed=k + n + off)
+
+
+# ------------------------------------------------------------------ dw
+DW_SIZES = [0, 1, 63, 64, 65, 200, 0, 130]   # sum 523
+
+
+@pytest.mark.parametrize("m,k,n,off,gl,limit", [(600, 136, 264, 0, 8, None), (600, 128, 256, 2, 5, 400),
+                                                (523, 264, 72, 0, 8, 523), (600, 64, 520, 3, 4, 130)])
+def test_dw(rd_lib, m, k, n, off, gl, limit):
+    run_dw(rd_lib, m, k, n, DW_SIZES, off=off, gl=gl, limit=limit, seed=k + n + off)
+
+
+def test_dw_all_groups_empty(rd_lib):
+    out = torch.empty((3, 128, 256), dtype=torch.bfloat16, device=DEV)
+    out.view(torch.int16).fill_(SENT)
+    x = torch.randn(64, 128, device=DEV).to(torch.bfloat16)
+    y = torch.randn(64, 256, device=DEV).to(torch.bfloat16)
+    rd_lib.trans_ragged_dot(x, y, _i32([10, 20, 34]), limit=_i32([0]), out=out)
+    torch.cuda.synchronize()
+    assert np.all(obf.torch_bf16_bits(out) == 0)
+
+
+# ------------------------------------------------------------------ structure
+def test_expert_parallel_shards_sum_to_full(rd_lib):
+    """Running each expert shard with its group_offset and summing gives the full forward."""
+    rng = np.random.default_rng(9)
+    m, k, n, g, shards = 1024, 128, 256, 8, 4
+    sizes = rng.multinomial(1000, np.full(g, 1 / g)).tolist()
+    lhs = _normal(rng, (m, k)).to(DEV)
+    rhs = _normal(rng, (g, k, n), 1 / k).to(DEV)
+    gs = _i32(sizes)
+    full = rd_lib.ragged_dot(lhs, rhs, gs)
+    gl = g // shards
+    parts = [rd_lib.ragged_dot(lhs, rhs[r * gl:(r + 1) * gl].contiguous(), gs, group_offset=r * gl)
+             for r in range(shards)]
+    total = sum(p.float() for p in parts)
+    torch.cuda.synchronize()
+    # every row belongs to exactly one shard, the others write +0 there: the sum is exact
+    assert torch.equal(total[:1000].to(torch.bfloat16), full[:1000])
+    dw = rd_lib.trans_ragged_dot(lhs, full, gs)
+    dws = torch.cat([rd_lib.trans_ragged_dot(lhs, full, gs, group_offset=r * gl, g_local=gl)
+                     for r in range(shards)])
+    torch.cuda.synchronize()
+    assert torch.equal(dw, dws)
+
+
+def test_cuda_graph_follows_device_group_sizes(rd_lib):
+    """Two calls sharing group_sizes captured in one graph; replays see new sizes."""
+    rng = np.random.default_rng(10)
+    m, k, n, g = 512, 128, 256, 4
+    lhs = _normal(rng, (m, k)).to(DEV)
+    up = _normal(rng, (g, k, 2 * n), 1 / k).to(DEV)
+    down = _normal(rng, (g, n, k), 1 / n).to(DEV)
+    gs = _i32([100, 0, 200, 212])
+    h = torch.empty((m, n), dtype=torch.bfloat16, device=DEV)
+    o = torch.empty((m, k), dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        rd_lib.ragged_dot(lhs, up, gs, epilogue=rd_lib.EPI_SILU_GLU, out=h)   # first calls outside capture
+        rd_lib.ragged_dot(h, down, gs, out=o)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        rd_lib.ragged_dot(lhs, up, gs, epilogue=rd_lib.EPI_SILU_GLU, out=h)
+        rd_lib.ragged_dot(h, down, gs, out=o)
+    for sizes in ([100, 0, 200, 212], [0, 512, 0, 0], [3, 1, 0, 508]):
+        gs.copy_(_i32(sizes))
+        graph.replay()
+        torch.cuda.synchronize()
+        ref_h = rd_lib.ragged_dot(lhs, up, gs, epilogue=rd_lib.EPI_SILU_GLU)
+        ref_o = rd_lib.ragged_dot(ref_h, down, gs)
+        torch.cuda.synchronize()
+        assert torch.equal(h, ref_h) and torch.equal(o, ref_o)
+        b, _ = oracle.group_bounds(sizes, m)
+        a64, w64 = _f64(lhs), _f64(up)
+        ref = oracle.ragged_dot(a64, w64, sizes, glu=True)
+        plain = oracle.ragged_dot(a64, w64, sizes)
+        E = 1e-3 * math.sqrt(k) * np.abs(a64).max() * np.abs(w64).max()
+        ref, tol = glu_epilogue_tol(plain[:, :n], plain[:, n:], E)
+        assert_close(_f64(h), ref, tol, f"graph replay sizes {sizes}")
