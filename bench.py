@@ -1,0 +1,557 @@
+#!/usr/bin/env python
+"""Benchmark of the ragged_dot (MoE grouped GEMM) hot path on GB300.
+
+Headline step: one rd_ragged_dot forward over the Mixtral-shaped workload
+(16384 tokens routed top-2 over 8 experts -> lhs [32768, 4096] bf16,
+rhs [8, 4096, 14336] bf16, out [32768, 14336] bf16, f32 accumulation).
+The metric is TFLOP/s over the valid rows (2 * rows * k * n per step); the
+inputs (2.15 GB moved per step) are larger than the 129 MB L2, so no flush
+is needed between steps.
+
+Also reported on the same line:
+  roofline      the kernel's achieved TFLOP/s (CUDA events on its stream)
+                against the measured bf16 dense peak;
+  e2e           the same metric through the C ABI with pinned host buffers,
+                host->device copies of the inputs and device->host copy of
+                the output inside the timed region;
+  cpu_baseline  the float64 oracle timed on a bounded sample of the same
+                workload on this host's cores;
+  ops           the other rows of the hot path at their own workloads
+                (packed GLU forward, dx, dw, decode pair in one CUDA graph,
+                standalone GLU forward/backward), each as time per call and
+                fraction of its roofline.
+
+--impl reference times the oracle itself as the reference arm.
+Under torchrun (--gpus N) every rank runs an independent replica (no
+data-path collective); times are max-reduced across ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- helpers
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.proc = None
+        self.gpu = gpu_index
+        self.period = period_ms
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        # median under load: samples at the upper half of the observed range
+        hi = sorted(sm)[len(sm) // 2:]
+        return {"sm_mhz": statistics.median(hi), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "expert_ffn_ragged_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if still current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    e = rec.get(kernel, {}).get(workload)
+    if not e or e.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+# ----------------------------------------------------------------- workloads
+def mixtral_inputs(device):
+    import torch
+
+    from workloads import mixtral_fwd, normal_bf16
+
+    w = mixtral_fwd()
+    lhs = normal_bf16((w.m, w.k), w.lhs_var, 20, device)
+    rhs = normal_bf16((w.g_total, w.k, w.n), w.rhs_var, 21, device)
+    gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=device)
+    return w, lhs, rhs, gs
+
+
+def fwd_flops(w, rows=None):
+    rows = int(w.group_sizes.sum()) if rows is None else rows
+    return 2.0 * rows * w.k * w.n
+
+
+def time_launches(fn, steps, warmup, stream):
+    """Per-launch CUDA-event durations (ms) on `stream`, plus the total (ms)."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    per = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return per, t0.elapsed_time(t1)
+
+
+# ----------------------------------------------------------------- oracle timing
+def oracle_sample_run(w, lhs, rhs, target_s: float, max_cols=None):
+    """Time the float64 oracle on a bounded sample of the Mixtral workload.
+
+    The sample keeps every row, every group and the full contraction length
+    and takes the first `cols` output columns; `cols` is grown until one run
+    takes about `target_s` seconds.  Returns (TFLOP/s, seconds, description).
+    """
+    import numpy as np
+    import torch
+
+    import oracle
+
+    a64 = lhs.float().cpu().numpy().astype(np.float64)
+    cols = 128
+    max_cols = w.n if max_cols is None else max_cols
+    while True:
+        w64 = rhs[:, :, :cols].float().cpu().numpy().astype(np.float64)
+        t = time.perf_counter()
+        oracle.ragged_dot(a64, w64, w.group_sizes)
+        dt = time.perf_counter() - t
+        if dt >= target_s / 4 or cols >= max_cols:
+            break
+        cols = min(max_cols, cols * 4)
+    # final measured run at the size that reaches about target_s
+    if dt < target_s and cols < max_cols:
+        cols = min(max_cols, max(8, int(cols * target_s / max(dt, 1e-3)) // 8 * 8))
+        w64 = rhs[:, :, :cols].float().cpu().numpy().astype(np.float64)
+        t = time.perf_counter()
+        oracle.ragged_dot(a64, w64, w.group_sizes)
+        dt = time.perf_counter() - t
+    flops = 2.0 * int(w.group_sizes.sum()) * w.k * cols
+    desc = (f"all {int(w.group_sizes.sum())} rows, all 8 groups, k={w.k}, first {cols} of "
+            f"{w.n} output columns ({flops / 1e12:.3f} TFLOP)")
+    return flops / dt / 1e12, dt, desc, cols
+
+
+# ----------------------------------------------------------------- other ops
+def run_ops(rd, device, stream, peaks):
+    """Each remaining hot-path row at its own workload: time per call and roofline fraction."""
+    import numpy as np
+    import torch
+
+    from workloads import backward_pair, decode_fwd, normal_bf16, packed_glu_fwd
+
+    P = peaks["bf16_tflops"] * 1e12
+    BW = peaks["hbm_gbs"] * 1e9
+    res = {}
+
+    def med(fn, steps=20, warmup=3):
+        per, _ = time_launches(fn, steps, warmup, stream)
+        return statistics.median(per) * 1e-3
+
+    with torch.cuda.stream(stream):
+        # packed buffer forward + fused GLU, group_offset 16 of 64, limit 126156
+        w = packed_glu_fwd()
+        lhs = normal_bf16((w.m, w.k), 1.0, 30, device)
+        rhs = normal_bf16((w.g_local, w.k, w.n), w.rhs_var, 31, device)
+        gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=device)
+        lim = torch.tensor([w.limit], dtype=torch.int32, device=device)
+        out = torch.empty((w.m, w.n // 2), dtype=torch.bfloat16, device=device)
+        b = np.concatenate([[0], np.cumsum(w.group_sizes)])
+        rows = int(b[w.group_offset + w.g_local] - b[w.group_offset])
+        F = 2.0 * rows * w.k * w.n
+        zero_rows = w.limit - rows
+        B = rows * w.k * 2 + w.g_local * w.k * w.n * 2 + w.limit * (w.n // 2) * 2 + 4 * w.g_total
+        t = med(lambda: rd.ragged_dot(lhs, rhs, gs, w.group_offset, lim, rd.EPI_SILU_GLU, out))
+        res["packed_glu_fwd"] = {"us": t * 1e6, "tflops": F / t / 1e12, "gbs": B / t / 1e9,
+                                 "bound": "tensor", "frac": max(F / P, B / BW) / t,
+                                 "local_rows": rows, "zero_rows": zero_rows}
+        # standalone GLU on the same packed buffer shape
+        fused = normal_bf16((w.m, 2 * 1024), 1.0, 32, device)
+        gout = torch.empty((w.m, 1024), dtype=torch.bfloat16, device=device)
+        t = med(lambda: rd.glu_fwd(fused, lim, gout))
+        Bg = w.limit * 1024 * 2 * 3
+        res["glu_fwd"] = {"us": t * 1e6, "gbs": Bg / t / 1e9, "bound": "hbm", "frac": Bg / BW / t}
+        dfused = torch.empty_like(fused)
+        t = med(lambda: rd.glu_bwd(fused, gout, lim, dfused))
+        Bb = w.limit * 1024 * 2 * 5
+        res["glu_bwd"] = {"us": t * 1e6, "gbs": Bb / t / 1e9, "bound": "hbm", "frac": Bb / BW / t}
+        del lhs, rhs, out, fused, gout, dfused
+        torch.cuda.empty_cache()
+
+        # backward pair: dx and dw
+        w = backward_pair()
+        x = normal_bf16((w.m, w.k), 1.0, 40, device)
+        do = normal_bf16((w.m, w.n), 1.0, 41, device)
+        wt = normal_bf16((w.g_total, w.k, w.n), w.rhs_var, 42, device)
+        gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=device)
+        dx = torch.empty((w.m, w.k), dtype=torch.bfloat16, device=device)
+        dw = torch.empty((w.g_total, w.k, w.n), dtype=torch.bfloat16, device=device)
+        F = 2.0 * w.m * w.k * w.n
+        live = int((w.group_sizes > 0).sum())
+        t = med(lambda: rd.ragged_dot_trans_rhs(do, wt, gs, out=dx))
+        B = w.m * w.n * 2 + live * w.k * w.n * 2 + w.m * w.k * 2
+        res["dx"] = {"us": t * 1e6, "tflops": F / t / 1e12, "bound": "tensor",
+                     "frac": max(F / P, B / BW) / t}
+        t = med(lambda: rd.trans_ragged_dot(x, do, gs, out=dw))
+        B = w.m * w.k * 2 + w.m * w.n * 2 + w.g_total * w.k * w.n * 2
+        res["dw"] = {"us": t * 1e6, "tflops": F / t / 1e12, "bound": "tensor",
+                     "frac": max(F / P, B / BW) / t}
+        del x, do, wt, dx, dw
+        torch.cuda.empty_cache()
+
+        # decode pair (up with GLU, down) sharing group_sizes inside one CUDA graph
+        for skew in (True, False):
+            w = decode_fwd(skewed=skew)
+            lhs = normal_bf16((w.m, w.k), 1.0, 50, device)
+            up = normal_bf16((w.g_total, w.k, w.n), w.rhs_var, 51, device)
+            down = normal_bf16((w.g_total, w.n // 2, w.k), 1.0 / (w.n // 2), 52, device)
+            gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=device)
+            h = torch.empty((w.m, w.n // 2), dtype=torch.bfloat16, device=device)
+            o = torch.empty((w.m, w.k), dtype=torch.bfloat16, device=device)
+
+            def pair():
+                rd.ragged_dot(lhs, up, gs, epilogue=rd.EPI_SILU_GLU, out=h)
+                rd.ragged_dot(h, down, gs, out=o)
+
+            pair()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                pair()
+            t_pair = med(g.replay, steps=50, warmup=5)
+            t_up = med(lambda: rd.ragged_dot(lhs, up, gs, epilogue=rd.EPI_SILU_GLU, out=h), 50, 5)
+            t_down = med(lambda: rd.ragged_dot(h, down, gs, out=o), 50, 5)
+            live = int((w.group_sizes > 0).sum())
+            B_up = w.m * w.k * 2 + live * w.k * w.n * 2 + w.m * (w.n // 2) * 2
+            B_dn = w.m * (w.n // 2) * 2 + live * (w.n // 2) * w.k * 2 + w.m * w.k * 2
+            tag = "decode_skewed" if skew else "decode_uniform"
+            res[tag] = {"graph_pair_us": t_pair * 1e6, "up_us": t_up * 1e6, "down_us": t_down * 1e6,
+                        "bound": "hbm", "live_groups": live,
+                        "up_frac": B_up / BW / t_up, "down_frac": B_dn / BW / t_down,
+                        "pair_frac": (B_up + B_dn) / BW / t_pair}
+            del lhs, up, down, h, o, g
+            torch.cuda.empty_cache()
+    return res
+
+
+# ----------------------------------------------------------------- arms
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if args.impl == "rd" else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def max_over_ranks(pg, value, device):
+    if pg is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args):
+    world, rank, local, pg = dist_setup(args)
+    if rank != 0:
+        return 0
+    import torch
+
+    w, lhs, rhs, gs = mixtral_inputs("cpu") if not torch.cuda.is_available() else \
+        mixtral_inputs(f"cuda:{local}")
+    # each step: the oracle on a bounded sample of the workload, sized so that
+    # the whole run (warm-up + timed steps) takes about two minutes
+    per_step = max(0.2, min(3.0, 120.0 / max(1, args.steps + args.warmup)))
+    _, _, desc, cols = oracle_sample_run(w, lhs, rhs, target_s=per_step)
+    import numpy as np
+
+    import oracle
+
+    a64 = lhs.float().cpu().numpy().astype(np.float64)
+    w64 = rhs[:, :, :cols].float().cpu().numpy().astype(np.float64)
+    flops = 2.0 * int(w.group_sizes.sum()) * w.k * cols
+    for _ in range(args.warmup):
+        oracle.ragged_dot(a64, w64, w.group_sizes)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.ragged_dot(a64, w64, w.group_sizes)
+    dt = (time.perf_counter() - t) / args.steps
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": "grouped-GEMM TFLOP/s (valid rows)", "value": value,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_rd(args):
+    import torch
+
+    world, rank, local, pg = dist_setup(args)
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import expert_ffn_ragged_gb300 as rd
+
+    rd.load()
+    peaks, peak_src = load_peaks()
+    stream = torch.cuda.Stream(device)
+    w, lhs, rhs, gs = mixtral_inputs(device)
+    out = torch.empty((w.m, w.n), dtype=torch.bfloat16, device=device)
+    flops = fwd_flops(w)
+    rows = int(w.group_sizes.sum())
+    alg_bytes = rows * w.k * 2 + w.g_total * w.k * w.n * 2 + rows * w.n * 2 + 4 * w.g_total
+
+    def step():
+        rd.ragged_dot(lhs, rhs, gs, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        if pg is not None:
+            pg.barrier()
+        with ClockSampler(local) as clk:
+            per, total_ms = time_launches(step, args.steps, 0, stream)
+        if pg is not None:
+            pg.barrier()
+    total_ms = max_over_ranks(pg, total_ms, device)
+    ms_per_step = total_ms / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    mean_launch = statistics.mean(per) * 1e-3
+    achieved = flops / mean_launch / 1e12
+    peak = peaks["bf16_tflops"]
+    traffic = recorded_traffic("grouped_gemm_fwd", w.name)
+
+    # end to end through the C ABI with pinned host buffers
+    h_lhs = lhs.cpu().pin_memory()
+    h_rhs = rhs.cpu().pin_memory()
+    h_gs = gs.cpu().pin_memory()
+    h_out = torch.empty((w.m, w.n), dtype=torch.bfloat16).pin_memory()
+    d_lhs, d_rhs, d_gs = torch.empty_like(lhs), torch.empty_like(rhs), torch.empty_like(gs)
+    del lhs, rhs
+    torch.cuda.empty_cache()
+
+    def e2e_step():
+        d_lhs.copy_(h_lhs, non_blocking=True)
+        d_rhs.copy_(h_rhs, non_blocking=True)
+        d_gs.copy_(h_gs, non_blocking=True)
+        rd.ragged_dot(d_lhs, d_rhs, d_gs, out=out, stream=stream)
+        h_out.copy_(out, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    with torch.cuda.stream(stream):
+        _, e2e_ms = time_launches(e2e_step, e2e_steps, 2, stream)
+    e2e_ms = max_over_ranks(pg, e2e_ms, device)
+    e2e_value = world * flops / (e2e_ms / e2e_steps * 1e-3) / 1e12
+    h2d = h_lhs.numel() * 2 + h_rhs.numel() * 2 + h_gs.numel() * 4
+    d2h = h_out.numel() * 2
+    del d_lhs, d_rhs, h_out
+    torch.cuda.empty_cache()
+
+    ops = None
+    if not args.no_ops and rank == 0:
+        ops = run_ops(rd, device, stream, peaks)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, desc, _ = oracle_sample_run(w, h_lhs, h_rhs, target_s=10.0)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": desc, "seconds": round(dt, 2)}
+
+    if rank == 0:
+        line = {
+            "metric": "grouped-GEMM TFLOP/s (valid rows)",
+            "value": value,
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms_per_step,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "m": w.m, "k": w.k, "n": w.n, "g": w.g_total,
+                       "valid_rows": rows, "group_sizes": w.group_sizes.tolist(),
+                       "l2": "inputs larger than L2 (2.15 GB per step), no flush",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_src} bf16_tflops (burst)",
+                         "algorithmic_bytes": alg_bytes,
+                         "kernel": "grouped_gemm_kernel<fwd>"},
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+            "ops": ops,
+        }
+        print(json.dumps(line))
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def run_profile(args):
+    """A few launches of one workload, for ncu (no extras, no host copies)."""
+    import torch
+
+    import expert_ffn_ragged_gb300 as rd
+    from workloads import normal_bf16
+
+    rd.load()
+    device = torch.device("cuda", 0)
+    import workloads
+
+    if args.profile == "mixtral":
+        w, lhs, rhs, gs = mixtral_inputs(device)
+        out = torch.empty((w.m, w.n), dtype=torch.bfloat16, device=device)
+        fn = lambda: rd.ragged_dot(lhs, rhs, gs, out=out)
+    elif args.profile == "mixtral_small":
+        # the Mixtral forward with 1/4 of the tokens (8192 rows): 1.3 GB on the device
+        w = workloads.mixtral_fwd()
+        sizes = (w.group_sizes // 4).astype("int32")
+        m = int(sizes.sum())
+        lhs = normal_bf16((m, w.k), 1.0, 20, device)
+        rhs = normal_bf16((w.g_total, w.k, w.n), w.rhs_var, 21, device)
+        gs = torch.tensor(sizes, dtype=torch.int32, device=device)
+        out = torch.empty((m, w.n), dtype=torch.bfloat16, device=device)
+        fn = lambda: rd.ragged_dot(lhs, rhs, gs, out=out)
+    else:
+        raise SystemExit(f"unknown profile workload {args.profile}")
+    for _ in range(args.steps):
+        fn()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": args.profile, "launches": args.steps}))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["rd", "reference"], default="rd")
+    ap.add_argument("--no-ops", action="store_true", help="skip the other hot-path rows")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", default=None, help="run only a few launches of a workload (for ncu)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.profile is None:
+        args.warmup = 3
+    if args.profile:
+        return run_profile(args)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_rd(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
