@@ -502,35 +502,72 @@ def run_rd(args):
 
 def run_profile(args):
     """A few launches of one workload, for ncu (no extras, no host copies)."""
+    import numpy as np
     import torch
 
     import expert_ffn_ragged_gb300 as rd
+    import workloads
     from workloads import normal_bf16
 
     rd.load()
     device = torch.device("cuda", 0)
-    import workloads
-
-    if args.profile == "mixtral":
-        w, lhs, rhs, gs = mixtral_inputs(device)
-        out = torch.empty((w.m, w.n), dtype=torch.bfloat16, device=device)
-        fn = lambda: rd.ragged_dot(lhs, rhs, gs, out=out)
-    elif args.profile == "mixtral_small":
-        # the Mixtral forward with 1/4 of the tokens (8192 rows): 1.3 GB on the device
+    name = args.profile
+    if name in ("mixtral", "mixtral_small"):
         w = workloads.mixtral_fwd()
-        sizes = (w.group_sizes // 4).astype("int32")
+        # mixtral_small: the same forward with a quarter of the tokens (8189 rows, 1.2 GB)
+        sizes = w.group_sizes if name == "mixtral" else (w.group_sizes // 4).astype("int32")
         m = int(sizes.sum())
         lhs = normal_bf16((m, w.k), 1.0, 20, device)
         rhs = normal_bf16((w.g_total, w.k, w.n), w.rhs_var, 21, device)
         gs = torch.tensor(sizes, dtype=torch.int32, device=device)
         out = torch.empty((m, w.n), dtype=torch.bfloat16, device=device)
         fn = lambda: rd.ragged_dot(lhs, rhs, gs, out=out)
+    elif name == "packed_glu":
+        w = workloads.packed_glu_fwd()
+        lhs = normal_bf16((w.m, w.k), 1.0, 30, device)
+        rhs = normal_bf16((w.g_local, w.k, w.n), w.rhs_var, 31, device)
+        gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=device)
+        lim = torch.tensor([w.limit], dtype=torch.int32, device=device)
+        out = torch.empty((w.m, w.n // 2), dtype=torch.bfloat16, device=device)
+        fn = lambda: rd.ragged_dot(lhs, rhs, gs, w.group_offset, lim, rd.EPI_SILU_GLU, out)
+    elif name in ("dx", "dw"):
+        w = workloads.backward_pair()
+        gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=device)
+        do = normal_bf16((w.m, w.n), 1.0, 41, device)
+        if name == "dx":
+            wt = normal_bf16((w.g_total, w.k, w.n), w.rhs_var, 42, device)
+            dx = torch.empty((w.m, w.k), dtype=torch.bfloat16, device=device)
+            fn = lambda: rd.ragged_dot_trans_rhs(do, wt, gs, out=dx)
+        else:
+            x = normal_bf16((w.m, w.k), 1.0, 40, device)
+            dw = torch.empty((w.g_total, w.k, w.n), dtype=torch.bfloat16, device=device)
+            fn = lambda: rd.trans_ragged_dot(x, do, gs, out=dw)
+    elif name in ("glu_fwd", "glu_bwd"):
+        w = workloads.packed_glu_fwd()
+        lim = torch.tensor([w.limit], dtype=torch.int32, device=device)
+        fused = normal_bf16((w.m, 2048), 1.0, 32, device)
+        gout = torch.empty((w.m, 1024), dtype=torch.bfloat16, device=device)
+        dfused = torch.empty_like(fused)
+        fn = (lambda: rd.glu_fwd(fused, lim, gout)) if name == "glu_fwd" else \
+            (lambda: rd.glu_bwd(fused, gout, lim, dfused))
+    elif name == "decode":
+        w = workloads.decode_fwd(True)
+        lhs = normal_bf16((w.m, w.k), 1.0, 50, device)
+        up = normal_bf16((w.g_total, w.k, w.n), w.rhs_var, 51, device)
+        down = normal_bf16((w.g_total, w.n // 2, w.k), 1.0 / (w.n // 2), 52, device)
+        gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=device)
+        h = torch.empty((w.m, w.n // 2), dtype=torch.bfloat16, device=device)
+        o = torch.empty((w.m, w.k), dtype=torch.bfloat16, device=device)
+
+        def fn():
+            rd.ragged_dot(lhs, up, gs, epilogue=rd.EPI_SILU_GLU, out=h)
+            rd.ragged_dot(h, down, gs, out=o)
     else:
-        raise SystemExit(f"unknown profile workload {args.profile}")
+        raise SystemExit(f"unknown profile workload {name}")
     for _ in range(args.steps):
         fn()
     torch.cuda.synchronize()
-    print(json.dumps({"profile": args.profile, "launches": args.steps}))
+    print(json.dumps({"profile": name, "launches": args.steps}))
     return 0
 
 

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "../../include/rd.h"
@@ -119,6 +121,21 @@ int grid_for(int sms, int64_t tiles_upper_bound) {
   return static_cast<int>(g < sms ? g : sms);
 }
 
+// Forward and dx run either on single CTAs (128x256 tiles) or on CTA pairs
+// (256x256 tiles, cta_group::2).  The pair variant is the default; the
+// environment variable RD_GEMM_VARIANT=single|pair forces one (for
+// measurements and tests of both).
+bool use_pair(int sms) {
+  if (sms < 2) return false;
+  const char* v = getenv("RD_GEMM_VARIANT");
+  if (v != nullptr && strcmp(v, "single") == 0) return false;
+  return true;
+}
+
+int pair_grid(int sms, int64_t pair_tiles_upper_bound) {
+  return 2 * grid_for(sms / 2, pair_tiles_upper_bound);
+}
+
 }  // namespace
 }  // namespace rd
 
@@ -177,8 +194,10 @@ extern "C" rd_status rd_ragged_dot(const void* lhs, const void* rhs, void* out, 
   a.n_tiles = static_cast<int32_t>((n_out + tile_w - 1) / tile_w);
   a.dw_m_tiles = 0;
   a.timeout_ns = kTimeoutNs;
-  const int grid = grid_for(sms, ((m + kBM - 1) / kBM + g_local) * a.n_tiles);
-  return launch_gemm_fwd(glu, ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) ==
+  const bool pair = use_pair(sms);
+  const int grid = pair ? pair_grid(sms, ((m + 2 * kBM - 1) / (2 * kBM) + g_local) * a.n_tiles)
+                        : grid_for(sms, ((m + kBM - 1) / kBM + g_local) * a.n_tiles);
+  return launch_gemm_fwd(glu, pair, ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? RD_OK
              : RD_ERR_CUDA;
@@ -204,6 +223,7 @@ extern "C" rd_status rd_ragged_dot_trans_rhs(const void* lhs, const void* rhs, v
   if ((st = current_device(&sms)) != RD_OK) return st;
   if (m == 0 || k == 0) return RD_OK;
 
+  const bool pair = use_pair(sms);
   CUtensorMap ta = {}, tb = {};
   if (n > 0) {
     const uint64_t da[2] = {static_cast<uint64_t>(n), static_cast<uint64_t>(m)};
@@ -213,7 +233,8 @@ extern "C" rd_status rd_ragged_dot_trans_rhs(const void* lhs, const void* rhs, v
     const uint64_t db[3] = {static_cast<uint64_t>(n), static_cast<uint64_t>(k),
                             static_cast<uint64_t>(g_local)};
     const uint64_t sb[2] = {static_cast<uint64_t>(n) * 2, static_cast<uint64_t>(k) * n * 2};
-    const uint32_t bb[3] = {64, kBN, 1};
+    // each CTA of a pair holds half of the 256 output columns
+    const uint32_t bb[3] = {64, static_cast<uint32_t>(pair ? kBN / 2 : kBN), 1};
     if ((st = encode(&tb, rhs, 3, db, sb, bb)) != RD_OK) return st;
   }
   GemmArgs a = {};
@@ -229,8 +250,10 @@ extern "C" rd_status rd_ragged_dot_trans_rhs(const void* lhs, const void* rhs, v
   a.g_local = g_local;
   a.n_tiles = static_cast<int32_t>((k + kBN - 1) / kBN);
   a.timeout_ns = kTimeoutNs;
-  const int grid = grid_for(sms, ((m + kBM - 1) / kBM + g_local) * a.n_tiles);
-  return launch_gemm_dx(ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+  const int grid = pair ? pair_grid(sms, ((m + 2 * kBM - 1) / (2 * kBM) + g_local) * a.n_tiles)
+                        : grid_for(sms, ((m + kBM - 1) / kBM + g_local) * a.n_tiles);
+  return launch_gemm_dx(pair, ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
              ? RD_OK
              : RD_ERR_CUDA;
 }

@@ -14,15 +14,12 @@ enum GemmOp : int {
   kOpDw = 2    // out[j] = x[rows_j]^T @ y[rows_j]     (A MN-major, B MN-major)
 };
 
-// UMMA tile: 128 x 256 f32 accumulator per tile, 64-deep K blocks (one
-// 128-byte swizzle atom of bf16), 4-stage shared-memory ring.
+// UMMA tile: 128 x 256 f32 accumulator per CTA, 64-deep K blocks (one
+// 128-byte swizzle atom of bf16).
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
 constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warps 6-7 zero fill
-constexpr int kStageBytesA = kBM * kBK * 2;
-constexpr int kStageBytesB = kBN * kBK * 2;
 constexpr int kTmemCols = 2 * kBN;  // two accumulators (double buffer)
 constexpr int kMaxGroups = 1024;
 
@@ -44,12 +41,12 @@ struct GemmArgs {
   uint64_t timeout_ns;         // bound of every wait inside the kernel
 };
 
-// shared memory the grouped-GEMM kernel needs (ring + bookkeeping + alignment slack)
-size_t gemm_smem_bytes();
-
-cudaError_t launch_gemm_fwd(bool glu, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                            const GemmArgs& args, int grid, cudaStream_t stream);
-cudaError_t launch_gemm_dx(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+// `pair`: the CTA-pair variant (clusters of two CTAs, 256-row tiles); `grid`
+// must then be even.
+cudaError_t launch_gemm_fwd(bool glu, bool pair, const CUtensorMap& tmap_a,
+                            const CUtensorMap& tmap_b, const GemmArgs& args, int grid,
+                            cudaStream_t stream);
+cudaError_t launch_gemm_dx(bool pair, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                            const GemmArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_gemm_dw(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                            const GemmArgs& args, int grid, cudaStream_t stream);

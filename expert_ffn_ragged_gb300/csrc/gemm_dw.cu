@@ -4,7 +4,6 @@
 namespace rd {
 cudaError_t launch_gemm_dw(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args,
                            int grid, cudaStream_t s) {
-  return launch_gemm_impl<kOpDw, false>(a, b, args, grid, s);
+  return launch_gemm_impl<kOpDw, false, false>(a, b, args, grid, s);
 }
-size_t gemm_smem_bytes() { return kGemmSmemBytes; }
 }  // namespace rd

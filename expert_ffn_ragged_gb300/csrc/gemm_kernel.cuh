@@ -11,23 +11,30 @@
 //   dw       out[j]  = x[rows_j]^T @ y[rows_j]
 //   rows in [0, L) outside the local groups are +0, rows >= L untouched.
 //
-// How (one CTA per SM, 256 threads):
+// How (persistent, 256 threads per CTA):
 //   * every CTA reads group_sizes and *limit itself and builds the group
 //     boundaries (exclusive prefix clamped to L) and the per-group tile
 //     prefix in shared memory -- no workspace, no host round trip;
-//   * tiles are handed out by static striding t = blockIdx.x + i * gridDim.x
-//     over (group, m-tile, n-tile) with m fastest, so the CTAs working at one
-//     time share each rhs column panel through L2;
-//   * warp 0 (one lane) streams A/B blocks with TMA into a 4-stage ring of
-//     128-byte-swizzled tiles; warp 1 issues tcgen05.mma 128x256x16 into one
-//     of two TMEM accumulators; warps 2-5 drain the other accumulator with
+//   * tiles are handed out by static striding over (group, m-tile, n-tile)
+//     with m fastest, so the CTAs working at one time share each rhs column
+//     panel through L2;
+//   * warp 0 (one lane) streams A/B blocks with TMA into a ring of
+//     128-byte-swizzled tiles; warp 1 issues tcgen05.mma into one of two
+//     TMEM accumulators; warps 2-5 drain the other accumulator with
 //     tcgen05.ld, round to bf16 (or apply the GLU) and store with row masks;
 //     warps 6-7 write the zero rows of the forward/dx outputs;
-//   * the last m-tile of a group is loaded from row (end - 128) so no row at
-//     or past the group end -- hence none at or past L -- is read; it stores
-//     only the rows it owns.  dw uses the same shift on its row (K) blocks and
-//     zeroes, in shared memory, the rows of a block that lie before the
-//     group, so rows of other groups never enter the sum (NaN-safe);
+//   * PAIR=false: one CTA per SM computes a 128x256 tile (UMMA 128x256x16,
+//     4-stage ring of 48 KB).  PAIR=true: a cluster of two CTAs computes a
+//     256x256 tile with the CTA-pair UMMA (cta_group::2, 256x256x16): each
+//     CTA loads its own 128 rows of A and its own 128 columns of B (32 KB per
+//     stage, 6 stages), both CTAs' copies are counted on the even CTA's
+//     barrier, the even CTA issues the MMA, and each CTA drains its own half
+//     of the accumulator.  Half the B bytes per SM and more stages in flight;
+//   * the last m-tile of a group is loaded from row (end - tile rows) so no
+//     row at or past the group end -- hence none at or past L -- is read; it
+//     stores only the rows it owns.  dw uses the same shift on its row (K)
+//     blocks, skips whole 16-row K steps before the group and zeroes, in
+//     shared memory, the rows of the straddling step (NaN-safe);
 //   * every wait is bounded; on expiry the CTA unwinds, drains its TMA and
 //     MMA work, frees TMEM and reports RD_STATUS_TIMEOUT.
 #pragma once
@@ -43,9 +50,21 @@
 
 namespace rd {
 
+template <bool PAIR>
+struct TileCfg {
+  static constexpr int kStagesN = PAIR ? 6 : 4;
+  static constexpr int kTileM = PAIR ? 2 * kBM : kBM;   // rows of one (pair) tile
+  static constexpr int kBCols = PAIR ? kBN / 2 : kBN;   // B columns held by one CTA
+  static constexpr int kStageA = kBM * kBK * 2;         // 16 KB
+  static constexpr int kStageB = kBCols * kBK * 2;      // 16 KB (pair) or 32 KB
+  static constexpr int kStageBytes = kStageA + kStageB;
+};
+
+template <bool PAIR>
 struct alignas(16) GemmShared {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  static constexpr int S = TileCfg<PAIR>::kStagesN;
+  uint64_t full[S];
+  uint64_t empty[S];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -59,8 +78,11 @@ struct alignas(16) GemmShared {
   int32_t tile_start[kMaxGroups + 1];  // first tile of each local group
 };
 
-constexpr size_t kGemmSmemBytes =
-    1024 + static_cast<size_t>(kStages) * (kStageBytesA + kStageBytesB) + sizeof(GemmShared);
+template <bool PAIR>
+constexpr size_t gemm_smem_bytes_t() {
+  return 1024 + static_cast<size_t>(TileCfg<PAIR>::kStagesN) * TileCfg<PAIR>::kStageBytes +
+         sizeof(GemmShared<PAIR>);
+}
 
 // One unit of work as every role sees it.
 struct Tile {
@@ -68,7 +90,7 @@ struct Tile {
   int32_t m_idx;     // row tile (fwd/dx: within the group; dw: within the weight block)
   int32_t n_idx;     // column tile
   int32_t rs, re;    // rows of the group, clamped to L
-  int32_t row_load;  // fwd/dx: first row the A tile is loaded from
+  int32_t row_load;  // fwd/dx: first row the tile's A rows are loaded from
   int32_t nkb;       // K blocks (0: the tile is all zeros)
 };
 
@@ -84,8 +106,9 @@ __device__ __forceinline__ long long warp_exclusive_scan(long long v, int lane) 
 }
 
 // Run by one warp: group boundaries, tile prefix, zero ranges, status bits.
-template <int OP, bool GLU>
-__device__ __forceinline__ void build_schedule(GemmShared& sh, const GemmArgs& a, int lane) {
+template <int OP, bool PAIR>
+__device__ __forceinline__ void build_schedule(GemmShared<PAIR>& sh, const GemmArgs& a, int lane) {
+  constexpr int TM = TileCfg<PAIR>::kTileM;
   int32_t L = a.m;
   if (a.limit != nullptr) {
     const int32_t v = *a.limit;
@@ -125,24 +148,17 @@ __device__ __forceinline__ void build_schedule(GemmShared& sh, const GemmArgs& a
   const int GL = a.g_local;
   const int per2 = (GL + 31) / 32;
   const int lo2 = min(lane * per2, GL), hi2 = min(lo2 + per2, GL);
+  auto tiles_of = [&](int j) -> long long {
+    if (OP == kOpDw) return static_cast<long long>(a.dw_m_tiles) * a.n_tiles;
+    const int cnt = sh.bound[a.group_offset + j + 1] - sh.bound[a.group_offset + j];
+    return static_cast<long long>((cnt + TM - 1) / TM) * a.n_tiles;
+  };
   long long tsum = 0;
-  for (int j = lo2; j < hi2; ++j) {
-    if (OP == kOpDw) {
-      tsum += static_cast<long long>(a.dw_m_tiles) * a.n_tiles;
-    } else {
-      const int cnt = sh.bound[a.group_offset + j + 1] - sh.bound[a.group_offset + j];
-      tsum += static_cast<long long>((cnt + kBM - 1) / kBM) * a.n_tiles;
-    }
-  }
+  for (int j = lo2; j < hi2; ++j) tsum += tiles_of(j);
   long long trun = warp_exclusive_scan(tsum, lane);
   for (int j = lo2; j < hi2; ++j) {
     sh.tile_start[j] = static_cast<int32_t>(trun);
-    if (OP == kOpDw) {
-      trun += static_cast<long long>(a.dw_m_tiles) * a.n_tiles;
-    } else {
-      const int cnt = sh.bound[a.group_offset + j + 1] - sh.bound[a.group_offset + j];
-      trun += static_cast<long long>((cnt + kBM - 1) / kBM) * a.n_tiles;
-    }
+    trun += tiles_of(j);
   }
   const long long ttotal = __shfl_sync(0xFFFFFFFFu, trun, 31);
   if (lane == 0) {
@@ -153,8 +169,9 @@ __device__ __forceinline__ void build_schedule(GemmShared& sh, const GemmArgs& a
   }
 }
 
-template <int OP>
-__device__ __forceinline__ Tile decode_tile(const GemmShared& sh, const GemmArgs& a, int t) {
+template <int OP, bool PAIR>
+__device__ __forceinline__ Tile decode_tile(const GemmShared<PAIR>& sh, const GemmArgs& a, int t) {
+  constexpr int TM = TileCfg<PAIR>::kTileM;
   Tile tl;
   if (OP == kOpDw) {
     const int per_group = a.dw_m_tiles * a.n_tiles;
@@ -176,11 +193,11 @@ __device__ __forceinline__ Tile decode_tile(const GemmShared& sh, const GemmArgs
     const int u = t - sh.tile_start[lo];
     tl.rs = sh.bound[a.group_offset + lo];
     tl.re = sh.bound[a.group_offset + lo + 1];
-    const int mt = (tl.re - tl.rs + kBM - 1) / kBM;
+    const int mt = (tl.re - tl.rs + TM - 1) / TM;
     tl.m_idx = u % mt;
     tl.n_idx = u / mt;
-    const int first = tl.rs + tl.m_idx * kBM;
-    tl.row_load = (tl.m_idx == mt - 1) ? tl.re - kBM : first;
+    const int first = tl.rs + tl.m_idx * TM;
+    tl.row_load = (tl.m_idx == mt - 1) ? tl.re - TM : first;
     tl.nkb = (a.kc + kBK - 1) / kBK;
   }
   return tl;
@@ -198,29 +215,37 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* row_ptr, int col, int
   }
 }
 
-template <int OP, bool GLU>
+template <int OP, bool GLU, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
+  using Cfg = TileCfg<PAIR>;
+  constexpr int S = Cfg::kStagesN;
+  constexpr int TM = Cfg::kTileM;
+  static_assert(!(PAIR && OP == kOpDw), "the pair variant covers the forward and dx");
+
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kStageBytesA;
-  GemmShared& sh = *reinterpret_cast<GemmShared*>(smem + kStages * (kStageBytesA + kStageBytesB));
+  uint8_t* sB = smem + S * Cfg::kStageA;
+  GemmShared<PAIR>& sh = *reinterpret_cast<GemmShared<PAIR>*>(smem + S * Cfg::kStageBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abort_flag = &sh.abort_flag;
+  const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;  // 0 = the CTA that issues the MMA
+  const int unit = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(ptx::smem_addr(&sh.full[s]), 1);
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(ptx::smem_addr(&sh.full[s]), PAIR ? 2 : 1);
       ptx::mbar_init(ptx::smem_addr(&sh.empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ptx::smem_addr(&sh.tfull[b]), 1);
-      ptx::mbar_init(ptx::smem_addr(&sh.tempty[b]), 4);
+      ptx::mbar_init(ptx::smem_addr(&sh.tempty[b]), PAIR ? 8 : 4);
     }
     ptx::mbar_init(ptx::smem_addr(&sh.drain), 1);
     sh.abort_flag = 0;
@@ -231,12 +256,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tmap_b);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(&sh.tmem_base), kTmemCols);
-    ptx::tmem_relinquish();
+    if (PAIR) {
+      ptx::tmem_alloc_pair(ptx::smem_addr(&sh.tmem_base), kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_addr(&sh.tmem_base), kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
-  if (warp == 2) build_schedule<OP, GLU>(sh, args, lane);
+  if (warp == 2) build_schedule<OP, PAIR>(sh, args, lane);
   ptx::tc_fence_before();
   __syncthreads();
+  if (PAIR) ptx::cluster_sync();  // the peer's barriers are initialised before any remote use
   ptx::tc_fence_after();
 
   const int total = sh.total_tiles;
@@ -247,149 +278,195 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t pend_mask = 0, pend_par = 0;
+      uint32_t pend_mask = 0, pend_par = 0;  // fills whose consumption is not yet seen
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<OP>(sh, args, t);
+      for (int t = unit; t < total && ok; t += units) {
+        const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
         for (int kb = 0; kb < tl.nkb; ++kb) {
-          if (!ptx::mbar_wait_bounded(ptx::smem_addr(&sh.empty[stage]), phase ^ 1, abort_flag,
-                                      tlimit)) {
+          if (!ptx::mbar_wait_bounded_t<PAIR>(ptx::smem_addr(&sh.empty[stage]), phase ^ 1,
+                                              abort_flag, tlimit)) {
             ok = false;
             break;
           }
           pend_mask &= ~(1u << stage);
-          const uint32_t fb = ptx::smem_addr(&sh.full[stage]);
-          ptx::mbar_arrive_expect_tx(fb, kStageBytesA + kStageBytesB);
-          const uint32_t a_dst = ptx::smem_addr(sA + stage * kStageBytesA);
-          const uint32_t b_dst = ptx::smem_addr(sB + stage * kStageBytesB);
-          if (OP == kOpFwd) {
-            ptx::tma_load_2d(a_dst, &tmap_a, fb, kb * kBK, tl.row_load);
+          const uint32_t fb_local = ptx::smem_addr(&sh.full[stage]);
+          const uint32_t a_dst = ptx::smem_addr(sA + stage * Cfg::kStageA);
+          const uint32_t b_dst = ptx::smem_addr(sB + stage * Cfg::kStageB);
+          if (PAIR) {
+            // both CTAs' bytes are counted on the even CTA's barrier
+            const uint32_t fb = ptx::map_to_rank(fb_local, 0);
+            if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, Cfg::kStageBytes);
+            else ptx::mbar_arrive_expect_tx_cluster(fb, Cfg::kStageBytes);
+            const int arow = tl.row_load + static_cast<int>(rank) * kBM;
+            ptx::tma_load_2d_pair(a_dst, &tmap_a, fb, kb * kBK, arow);
+            if (OP == kOpFwd) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int x = GLU ? ((c < 2 ? 0 : args.glu_f) + tl.n_idx * (kBN / 2) + (c & 1) * 64)
-                                : (tl.n_idx * kBN + c * 64);
-              ptx::tma_load_3d(b_dst + c * (kBK * 128), &tmap_b, fb, x, kb * kBK, tl.j);
+              for (int c = 0; c < 2; ++c) {
+                const int x = GLU ? ((rank == 0 ? 0 : args.glu_f) + tl.n_idx * (kBN / 2) + c * 64)
+                                  : (tl.n_idx * kBN + static_cast<int>(rank) * (kBN / 2) + c * 64);
+                ptx::tma_load_3d_pair(b_dst + c * (kBK * 128), &tmap_b, fb, x, kb * kBK, tl.j);
+              }
+            } else {
+              ptx::tma_load_3d_pair(b_dst, &tmap_b, fb, kb * kBK,
+                                    tl.n_idx * kBN + static_cast<int>(rank) * (kBN / 2), tl.j);
             }
-          } else if (OP == kOpDx) {
-            ptx::tma_load_2d(a_dst, &tmap_a, fb, kb * kBK, tl.row_load);
-            ptx::tma_load_3d(b_dst, &tmap_b, fb, kb * kBK, tl.n_idx * kBN, tl.j);
           } else {
-            const int row0 = (kb == tl.nkb - 1) ? tl.re - kBK : tl.rs + kb * kBK;
+            const uint32_t fb = fb_local;
+            ptx::mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+            if (OP == kOpFwd) {
+              ptx::tma_load_2d(a_dst, &tmap_a, fb, kb * kBK, tl.row_load);
 #pragma unroll
-            for (int c = 0; c < 2; ++c)
-              ptx::tma_load_2d(a_dst + c * (kBK * 128), &tmap_a, fb, tl.m_idx * kBM + c * 64, row0);
+              for (int c = 0; c < 4; ++c) {
+                const int x = GLU ? ((c < 2 ? 0 : args.glu_f) + tl.n_idx * (kBN / 2) + (c & 1) * 64)
+                                  : (tl.n_idx * kBN + c * 64);
+                ptx::tma_load_3d(b_dst + c * (kBK * 128), &tmap_b, fb, x, kb * kBK, tl.j);
+              }
+            } else if (OP == kOpDx) {
+              ptx::tma_load_2d(a_dst, &tmap_a, fb, kb * kBK, tl.row_load);
+              ptx::tma_load_3d(b_dst, &tmap_b, fb, kb * kBK, tl.n_idx * kBN, tl.j);
+            } else {
+              const int row0 = (kb == tl.nkb - 1) ? tl.re - kBK : tl.rs + kb * kBK;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              ptx::tma_load_2d(b_dst + c * (kBK * 128), &tmap_b, fb, tl.n_idx * kBN + c * 64, row0);
+              for (int c = 0; c < 2; ++c)
+                ptx::tma_load_2d(a_dst + c * (kBK * 128), &tmap_a, fb, tl.m_idx * kBM + c * 64, row0);
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                ptx::tma_load_2d(b_dst + c * (kBK * 128), &tmap_b, fb, tl.n_idx * kBN + c * 64, row0);
+            }
           }
           pend_mask |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) {
+          if (++stage == S) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
-      if (*abort_flag) {
-        // let every copy still in flight land before the CTA's shared memory goes away
-        volatile int no_abort = 0;
-        for (int s = 0; s < kStages; ++s)
-          if (pend_mask & (1u << s))
-            ptx::mbar_wait_bounded(ptx::smem_addr(&sh.full[s]), (pend_par >> s) & 1u, &no_abort,
-                                   tlimit);
+      // Wait until every fill of this CTA's ring has been consumed, so that no MMA
+      // commit (possibly from the peer CTA) arrives on a barrier after this CTA exits.
+      // On abort, wait (bounded) for the copies still in flight instead.
+      volatile int no_abort = 0;
+      for (int s = 0; s < S; ++s) {
+        if (!(pend_mask & (1u << s))) continue;
+        const uint32_t par = (pend_par >> s) & 1u;
+        if (*abort_flag) {
+          if (!PAIR || rank == 0)
+            ptx::mbar_wait_bounded(ptx::smem_addr(&sh.full[s]), par, &no_abort, tlimit);
+        } else {
+          ptx::mbar_wait_bounded_t<PAIR>(ptx::smem_addr(&sh.empty[s]), par, &no_abort, tlimit);
+        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr bool a_mn = (OP == kOpDw);
-    constexpr bool b_mn = (OP != kOpDx);
-    constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, kBN, a_mn, b_mn);
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile tl = decode_tile<OP>(sh, args, t);
-      if (tl.nkb == 0) continue;
-      ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.tempty[acc]), acc_phase ^ 1, abort_flag,
-                                  tlimit);
-      ok = __all_sync(0xFFFFFFFFu, ok);
-      if (!ok) break;
-      ptx::tc_fence_after();
-      const uint32_t d_tmem = sh.tmem_base + static_cast<uint32_t>(acc * kBN);
-      for (int kb = 0; kb < tl.nkb; ++kb) {
-        ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.full[stage]), phase, abort_flag, tlimit);
+    if (!PAIR || rank == 0) {
+      constexpr bool a_mn = (OP == kOpDw);
+      constexpr bool b_mn = (OP != kOpDx);
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(TM, kBN, a_mn, b_mn);
+      constexpr uint32_t b_lbo = kBK * 128;  // MN-major B: stride between 64-wide chunks
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int t = unit; t < total && ok; t += units) {
+        const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
+        if (tl.nkb == 0) continue;
+        ok = ptx::mbar_wait_bounded_t<PAIR>(ptx::smem_addr(&sh.tempty[acc]), acc_phase ^ 1,
+                                            abort_flag, tlimit);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
         ptx::tc_fence_after();
-        uint8_t* a_st = sA + stage * kStageBytesA;
-        uint8_t* b_st = sB + stage * kStageBytesB;
-        if (OP == kOpDw && kb == tl.nkb - 1) {
-          // rows of the last block that precede this group's block start: zero them in
-          // both operands so nothing from a neighbouring group (or a NaN) enters the sum
-          const int rem = (tl.re - tl.rs) - (tl.nkb - 1) * kBK;
-          const int zrows = kBK - rem;
-          if (zrows > 0) {
-            // each row is one 128-byte line per 64-wide chunk: 2 chunks of A, 4 of B
-            const int units = zrows * 6 * 8;  // 16-byte units
-            for (int u = lane; u < units; u += 32) {
-              const int row = u / 48;
-              const int rest = u - row * 48;
-              const int chunk = rest >> 3;
-              const int part = rest & 7;
-              uint8_t* base = chunk < 2 ? a_st + chunk * (kBK * 128)
-                                        : b_st + (chunk - 2) * (kBK * 128);
-              *reinterpret_cast<uint4*>(base + row * 128 + part * 16) = make_uint4(0, 0, 0, 0);
+        const uint32_t d_tmem = sh.tmem_base + static_cast<uint32_t>(acc * kBN);
+        for (int kb = 0; kb < tl.nkb; ++kb) {
+          ok = ptx::mbar_wait_bounded_t<PAIR>(ptx::smem_addr(&sh.full[stage]), phase, abort_flag,
+                                              tlimit);
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          uint8_t* a_st = sA + stage * Cfg::kStageA;
+          uint8_t* b_st = sB + stage * Cfg::kStageB;
+          int kk0 = 0;  // first 16-deep K step issued for this block
+          if (OP == kOpDw && kb == tl.nkb - 1) {
+            // The last block was loaded from row (end - 64); its first zrows rows precede
+            // the block's own start.  Whole 16-row K steps of them are skipped; the rows of
+            // the straddling step are zeroed in both operands so nothing from a
+            // neighbouring group (or a NaN) enters the sum.
+            const int rem = (tl.re - tl.rs) - (tl.nkb - 1) * kBK;
+            const int zrows = kBK - rem;
+            kk0 = zrows >> 4;
+            const int z0 = kk0 << 4;
+            if (zrows > z0) {
+              // each row is one 128-byte line per 64-wide chunk: 2 chunks of A, 4 of B
+              const int nunits = (zrows - z0) * 6 * 8;  // 16-byte units
+              for (int u = lane; u < nunits; u += 32) {
+                const int row = z0 + u / 48;
+                const int rest = u % 48;
+                const int chunk = rest >> 3;
+                const int part = rest & 7;
+                uint8_t* base = chunk < 2 ? a_st + chunk * (kBK * 128)
+                                          : b_st + (chunk - 2) * (kBK * 128);
+                *reinterpret_cast<uint4*>(base + row * 128 + part * 16) = make_uint4(0, 0, 0, 0);
+              }
+              ptx::fence_proxy_async_smem();
             }
-            ptx::fence_proxy_async_smem();
+            __syncwarp();
+          }
+          if (lane == 0) {
+            const uint32_t a_addr = ptx::smem_addr(a_st);
+            const uint32_t b_addr = ptx::smem_addr(b_st);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              if (kk < kk0) continue;
+              const uint64_t adesc = a_mn ? ptx::sw128_desc(a_addr + kk * 2048, kBK * 128, 1024)
+                                          : ptx::sw128_desc(a_addr + kk * 32, 16, 1024);
+              const uint64_t bdesc = b_mn ? ptx::sw128_desc(b_addr + kk * 2048, b_lbo, 1024)
+                                          : ptx::sw128_desc(b_addr + kk * 32, 16, 1024);
+              const uint32_t accum = (kb > 0 || kk > kk0) ? 1u : 0u;
+              if (PAIR) ptx::tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, accum);
+              else ptx::tc_mma_bf16(d_tmem, adesc, bdesc, idesc, accum);
+            }
+            if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&sh.empty[stage]), 0x3);
+            else ptx::tc_commit(ptx::smem_addr(&sh.empty[stage]));
           }
           __syncwarp();
-        }
-        if (lane == 0) {
-          const uint32_t a_addr = ptx::smem_addr(a_st);
-          const uint32_t b_addr = ptx::smem_addr(b_st);
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t adesc = a_mn ? ptx::sw128_desc(a_addr + kk * 2048, kBK * 128, 1024)
-                                        : ptx::sw128_desc(a_addr + kk * 32, 16, 1024);
-            const uint64_t bdesc = b_mn ? ptx::sw128_desc(b_addr + kk * 2048, kBK * 128, 1024)
-                                        : ptx::sw128_desc(b_addr + kk * 32, 16, 1024);
-            ptx::tc_mma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
           }
-          ptx::tc_commit(ptx::smem_addr(&sh.empty[stage]));
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&sh.tfull[acc]), 0x3);
+          else ptx::tc_commit(ptx::smem_addr(&sh.tfull[acc]));
         }
         __syncwarp();
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1;
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (*abort_flag) {
+        // wait until every MMA this thread issued has completed before TMEM is freed
+        if (lane == 0) {
+          volatile int no_abort = 0;
+          if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&sh.drain), 0x1);
+          else ptx::tc_commit(ptx::smem_addr(&sh.drain));
+          ptx::mbar_wait_bounded(ptx::smem_addr(&sh.drain), 0, &no_abort, tlimit);
         }
+        __syncwarp();
       }
-      if (!ok) break;
-      if (lane == 0) ptx::tc_commit(ptx::smem_addr(&sh.tfull[acc]));
-      __syncwarp();
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
-    }
-    if (*abort_flag) {
-      // wait until every MMA this thread issued has completed before TMEM is freed
-      if (lane == 0) {
-        volatile int no_abort = 0;
-        ptx::tc_commit(ptx::smem_addr(&sh.drain));
-        ptx::mbar_wait_bounded(ptx::smem_addr(&sh.drain), 0, &no_abort, tlimit);
-      }
-      __syncwarp();
     }
   } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int r_in_tile = q * 32 + lane;
+    const int r_in_tile = static_cast<int>(rank) * kBM + q * 32 + lane;
     constexpr int tile_w = GLU ? kBN / 2 : kBN;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
+    const uint32_t tempty_leader =
+        PAIR ? ptx::map_to_rank(ptx::smem_addr(&sh.tempty[0]), 0) : 0u;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile<OP>(sh, args, t);
+    for (int t = unit; t < total; t += units) {
+      const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
       // destination row of this thread and whether it owns it
       int row;
       bool valid;
@@ -400,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         row_ptr = out + (static_cast<size_t>(tl.j) * args.m_out + row) * args.n_out;
       } else {
         row = tl.row_load + r_in_tile;
-        valid = row >= tl.rs + tl.m_idx * kBM && row < tl.re;
+        valid = row >= tl.rs + tl.m_idx * TM && row < tl.re;
         row_ptr = out + static_cast<size_t>(row) * args.n_out;
       }
       const int col0 = tl.n_idx * tile_w;
@@ -410,8 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < tile_w / 32; ++c) store_row32(row_ptr, col0 + c * 32, args.n_out, z);
         continue;
       }
-      bool ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.tfull[acc]), acc_phase, abort_flag,
-                                       tlimit);
+      bool ok = ptx::mbar_wait_bounded_t<PAIR>(ptx::smem_addr(&sh.tfull[acc]), acc_phase,
+                                               abort_flag, tlimit);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
@@ -443,7 +520,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&sh.tempty[acc]));
+      if (lane == 0) {
+        if (PAIR && rank != 0)
+          ptx::mbar_arrive_cluster(tempty_leader + static_cast<uint32_t>(acc * sizeof(uint64_t)));
+        else
+          ptx::mbar_arrive(ptx::smem_addr(&sh.tempty[acc]));
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -466,27 +548,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
+  if (PAIR) ptx::cluster_sync();  // the peer no longer touches this CTA's barriers or TMEM
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(sh.tmem_base, kTmemCols);
+    if (PAIR) ptx::tmem_dealloc_pair(sh.tmem_base, kTmemCols);
+    else ptx::tmem_dealloc(sh.tmem_base, kTmemCols);
   }
   if (threadIdx.x == 0 && sh.abort_flag && args.status != nullptr)
     atomicOr(args.status, RD_STATUS_TIMEOUT);
 }
 
-template <int OP, bool GLU>
+template <int OP, bool GLU, bool PAIR>
 cudaError_t launch_gemm_impl(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                              const GemmArgs& args, int grid, cudaStream_t stream) {
+  constexpr size_t smem = gemm_smem_bytes_t<PAIR>();
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<OP, GLU>,
+    const cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<OP, GLU, PAIR>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(kGemmSmemBytes));
+                                               static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  grouped_gemm_kernel<OP, GLU><<<grid, kThreads, kGemmSmemBytes, stream>>>(tmap_a, tmap_b, args);
-  return cudaGetLastError();
+  if (!PAIR) {
+    grouped_gemm_kernel<OP, GLU, PAIR><<<grid, kThreads, smem, stream>>>(tmap_a, tmap_b, args);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<OP, GLU, PAIR>, tmap_a, tmap_b, args);
 }
 
 }  // namespace rd

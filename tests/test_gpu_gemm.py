@@ -1,6 +1,6 @@
 """GPU parity of the grouped GEMMs against the float64 oracle, through the C ABI.
 
-Small shapes that span several 128x256 tiles and ragged edges in every
+Small shapes that span several 128x256 / 256x256 tiles and ragged edges in every
 dimension: group sizes 0, 1, BM-1, BM, BM+1, k and n not multiples of the
 tile, group offsets, valid-row limits, NaN-poisoned input rows past the
 limit, sentinel-filled output rows past the limit and canary rows after the
@@ -22,6 +22,13 @@ DEV = "cuda"
 SENT = 0x3C3C          # sentinel bf16 pattern for rows that must stay untouched
 CANARY_ROWS = 4
 EDGE_SIZES = [0, 1, 127, 128, 129, 0, 255, 3]   # sum 643
+
+
+@pytest.fixture(params=["pair", "single"], autouse=True)
+def gemm_variant(request, monkeypatch):
+    """Every test runs on both the CTA-pair (256-row) and the single-CTA (128-row) kernels."""
+    monkeypatch.setenv("RD_GEMM_VARIANT", request.param)
+    return request.param
 
 
 def _normal(rng, shape, var=1.0):
@@ -156,6 +163,16 @@ def test_tiny_workload(rd_lib):
 @pytest.mark.parametrize("m,k,n", [(700, 136, 264), (700, 64, 512), (643, 520, 256)])
 def test_forward_ragged_edges(rd_lib, m, k, n):
     run_fwd(rd_lib, m, k, n, EDGE_SIZES, seed=m + k + n)
+
+
+PAIR_EDGE_SIZES = [256, 257, 511, 1, 0, 513, 255]   # sum 1793: edges of 256-row tiles
+
+
+@pytest.mark.parametrize("limit", [None, 1500, 255])
+def test_forward_pair_tile_edges(rd_lib, limit):
+    run_fwd(rd_lib, 1800, 128, 512, PAIR_EDGE_SIZES, limit=limit, seed=11)
+    run_fwd(rd_lib, 1800, 64, 256, PAIR_EDGE_SIZES, off=1, gl=5, limit=limit, glu=True, seed=12)
+    run_dx(rd_lib, 1800, 512, 128, PAIR_EDGE_SIZES, off=2, gl=4, limit=limit, seed=13)
 
 
 @pytest.mark.parametrize("off,gl,limit", [(2, 4, None), (2, 4, 500), (0, 8, 300), (7, 1, None),
