@@ -122,14 +122,18 @@ int grid_for(int sms, int64_t tiles_upper_bound) {
 }
 
 // Forward and dx run either on single CTAs (128x256 tiles) or on CTA pairs
-// (256x256 tiles, cta_group::2).  The pair variant is the default; the
-// environment variable RD_GEMM_VARIANT=single|pair forces one (for
-// measurements and tests of both).
-bool use_pair(int sms) {
+// (256x256 tiles, cta_group::2).  Pairs halve the operand bytes each SM pulls
+// per MMA and win when groups are large; with small groups (decode-shaped
+// calls, a few rows per expert) the 256-row tile mostly computes padding and
+// single CTAs stream the weights faster.  The choice uses host-known shapes
+// only: pairs when the buffer holds at least 512 rows per group on average.
+// RD_GEMM_VARIANT=single|pair overrides it (for measurements and tests).
+bool use_pair(int sms, int64_t m, int32_t g_total) {
   if (sms < 2) return false;
   const char* v = getenv("RD_GEMM_VARIANT");
   if (v != nullptr && strcmp(v, "single") == 0) return false;
-  return true;
+  if (v != nullptr && strcmp(v, "pair") == 0) return true;
+  return m >= 512 * static_cast<int64_t>(g_total);
 }
 
 int pair_grid(int sms, int64_t pair_tiles_upper_bound) {
@@ -194,7 +198,7 @@ extern "C" rd_status rd_ragged_dot(const void* lhs, const void* rhs, void* out, 
   a.n_tiles = static_cast<int32_t>((n_out + tile_w - 1) / tile_w);
   a.dw_m_tiles = 0;
   a.timeout_ns = kTimeoutNs;
-  const bool pair = use_pair(sms);
+  const bool pair = use_pair(sms, m, g_total);
   const int grid = pair ? pair_grid(sms, ((m + 2 * kBM - 1) / (2 * kBM) + g_local) * a.n_tiles)
                         : grid_for(sms, ((m + kBM - 1) / kBM + g_local) * a.n_tiles);
   return launch_gemm_fwd(glu, pair, ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) ==
@@ -223,7 +227,7 @@ extern "C" rd_status rd_ragged_dot_trans_rhs(const void* lhs, const void* rhs, v
   if ((st = current_device(&sms)) != RD_OK) return st;
   if (m == 0 || k == 0) return RD_OK;
 
-  const bool pair = use_pair(sms);
+  const bool pair = use_pair(sms, m, g_total);
   CUtensorMap ta = {}, tb = {};
   if (n > 0) {
     const uint64_t da[2] = {static_cast<uint64_t>(n), static_cast<uint64_t>(m)};

@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(ptx::smem_addr(&sh.full[s]), PAIR ? 2 : 1);
+      ptx::mbar_init(ptx::smem_addr(&sh.full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&sh.empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = unit; t < total && ok; t += units) {
         const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
         for (int kb = 0; kb < tl.nkb; ++kb) {
-          if (!ptx::mbar_wait_bounded_t<PAIR>(ptx::smem_addr(&sh.empty[stage]), phase ^ 1,
+          if (!ptx::mbar_wait_bounded(ptx::smem_addr(&sh.empty[stage]), phase ^ 1,
                                               abort_flag, tlimit)) {
             ok = false;
             break;
@@ -293,10 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t a_dst = ptx::smem_addr(sA + stage * Cfg::kStageA);
           const uint32_t b_dst = ptx::smem_addr(sB + stage * Cfg::kStageB);
           if (PAIR) {
-            // both CTAs' bytes are counted on the even CTA's barrier
+            // Both CTAs' bytes are counted on the even CTA's barrier, which expects them
+            // all; the odd CTA's copies may land before that expectation is posted (the
+            // phase cannot complete before the even CTA's arrival).
             const uint32_t fb = ptx::map_to_rank(fb_local, 0);
-            if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, Cfg::kStageBytes);
-            else ptx::mbar_arrive_expect_tx_cluster(fb, Cfg::kStageBytes);
+            if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, 2 * Cfg::kStageBytes);
             const int arow = tl.row_load + static_cast<int>(rank) * kBM;
             ptx::tma_load_2d_pair(a_dst, &tmap_a, fb, kb * kBK, arow);
             if (OP == kOpFwd) {
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!PAIR || rank == 0)
             ptx::mbar_wait_bounded(ptx::smem_addr(&sh.full[s]), par, &no_abort, tlimit);
         } else {
-          ptx::mbar_wait_bounded_t<PAIR>(ptx::smem_addr(&sh.empty[s]), par, &no_abort, tlimit);
+          ptx::mbar_wait_bounded(ptx::smem_addr(&sh.empty[s]), par, &no_abort, tlimit);
         }
       }
     }
@@ -372,14 +373,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = unit; t < total && ok; t += units) {
         const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
         if (tl.nkb == 0) continue;
-        ok = ptx::mbar_wait_bounded_t<PAIR>(ptx::smem_addr(&sh.tempty[acc]), acc_phase ^ 1,
+        ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.tempty[acc]), acc_phase ^ 1,
                                             abort_flag, tlimit);
         ok = __all_sync(0xFFFFFFFFu, ok);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = sh.tmem_base + static_cast<uint32_t>(acc * kBN);
         for (int kb = 0; kb < tl.nkb; ++kb) {
-          ok = ptx::mbar_wait_bounded_t<PAIR>(ptx::smem_addr(&sh.full[stage]), phase, abort_flag,
+          ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.full[stage]), phase, abort_flag,
                                               tlimit);
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) break;
@@ -487,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < tile_w / 32; ++c) store_row32(row_ptr, col0 + c * 32, args.n_out, z);
         continue;
       }
-      bool ok = ptx::mbar_wait_bounded_t<PAIR>(ptx::smem_addr(&sh.tfull[acc]), acc_phase,
+      bool ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.tfull[acc]), acc_phase,
                                                abort_flag, tlimit);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
@@ -575,7 +576,6 @@ cudaError_t launch_gemm_impl(const CUtensorMap& tmap_a, const CUtensorMap& tmap_
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -586,6 +586,21 @@ cudaError_t launch_gemm_impl(const CUtensorMap& tmap_a, const CUtensorMap& tmap_
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  // A persistent grid must not exceed the clusters that can be resident at once:
+  // a CTA pair must sit in one GPC, so fewer than (#SMs / 2) pairs may fit.  The
+  // limit is queried once per device (it depends only on the kernel and the GPU).
+  static int max_clusters[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_clusters[dev] == 0) {
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    int n = 0;
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<OP, GLU, PAIR>, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters[dev] = n > 0 ? n : 1;
+  }
+  if (grid > 2 * max_clusters[dev]) grid = 2 * max_clusters[dev];
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<OP, GLU, PAIR>, tmap_a, tmap_b, args);
 }
 

@@ -8,7 +8,7 @@
 // the -0 -> +0 fix.  The arithmetic is in glu_math.cuh.
 //
 // Both kernels are HBM-bound streams: one warp per row, 16-byte vector loads
-// that bypass L1, up to four vectors per lane in flight before the math.
+// that bypass L1, several vectors per lane in flight before the math.
 // The row count L is read on the device, so no host round trip is needed and
 // the launch shape depends only on host-known sizes.
 #include <cuda_runtime.h>
@@ -22,7 +22,8 @@ namespace {
 
 constexpr int kGluThreads = 256;
 constexpr int kGluWarps = kGluThreads / 32;
-constexpr int kGluBatch = 4;
+constexpr int kFwdBatch = 4;  // 16-byte vectors per lane in flight before the math
+constexpr int kBwdBatch = 2;  // the backward holds three inputs per vector
 
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
   uint4 v;
@@ -63,10 +64,10 @@ __global__ void __launch_bounds__(kGluThreads) glu_fwd_kernel(const uint4* __res
     const uint4* g_row = fused + static_cast<size_t>(r) * 2 * vpr;
     const uint4* u_row = g_row + vpr;
     uint4* o_row = out + static_cast<size_t>(r) * vpr;
-    for (int v0 = lane; v0 < vpr; v0 += 32 * kGluBatch) {
-      uint4 g[kGluBatch], u[kGluBatch];
+    for (int v0 = lane; v0 < vpr; v0 += 32 * kFwdBatch) {
+      uint4 g[kFwdBatch], u[kFwdBatch];
 #pragma unroll
-      for (int b = 0; b < kGluBatch; ++b) {
+      for (int b = 0; b < kFwdBatch; ++b) {
         const int v = v0 + 32 * b;
         if (v < vpr) {
           g[b] = ld_stream(g_row + v);
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(kGluThreads) glu_fwd_kernel(const uint4* __res
         }
       }
 #pragma unroll
-      for (int b = 0; b < kGluBatch; ++b) {
+      for (int b = 0; b < kFwdBatch; ++b) {
         const int v = v0 + 32 * b;
         if (v < vpr)
           o_row[v] = make_uint4(glu2(g[b].x, u[b].x), glu2(g[b].y, u[b].y), glu2(g[b].z, u[b].z),
@@ -99,10 +100,10 @@ __global__ void __launch_bounds__(kGluThreads) glu_bwd_kernel(const uint4* __res
     const uint4* d_row = d_out + static_cast<size_t>(r) * vpr;
     uint4* dg_row = d_fused + static_cast<size_t>(r) * 2 * vpr;
     uint4* du_row = dg_row + vpr;
-    for (int v0 = lane; v0 < vpr; v0 += 32 * kGluBatch) {
-      uint4 g[kGluBatch], u[kGluBatch], d[kGluBatch];
+    for (int v0 = lane; v0 < vpr; v0 += 32 * kBwdBatch) {
+      uint4 g[kBwdBatch], u[kBwdBatch], d[kBwdBatch];
 #pragma unroll
-      for (int b = 0; b < kGluBatch; ++b) {
+      for (int b = 0; b < kBwdBatch; ++b) {
         const int v = v0 + 32 * b;
         if (v < vpr) {
           g[b] = ld_stream(g_row + v);
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(kGluThreads) glu_bwd_kernel(const uint4* __res
         }
       }
 #pragma unroll
-      for (int b = 0; b < kGluBatch; ++b) {
+      for (int b = 0; b < kBwdBatch; ++b) {
         const int v = v0 + 32 * b;
         if (v < vpr) {
           uint4 og, ou;

@@ -100,45 +100,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t remote_bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
-                   remote_bar),
-               "r"(bytes)
-               : "memory");
-}
-
-// try_wait with acquire at cluster scope, for barriers other CTAs arrive on
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-template <bool CLUSTER>
-__device__ __forceinline__ bool mbar_wait_bounded_t(uint32_t bar, uint32_t parity,
-                                                    volatile int* abort_flag, uint64_t limit_ns) {
-  auto poll = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
-#pragma unroll 1
-  for (int i = 0; i < 16; ++i)
-    if (poll()) return true;
-  const uint64_t t0 = global_timer_ns();
-#pragma unroll 1
-  while (true) {
-    if (poll()) return true;
-    if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > limit_ns) {
-      *abort_flag = 1;
-      return false;
-    }
-  }
-}
-
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
