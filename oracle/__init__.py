@@ -15,6 +15,7 @@ float64 unless the pages fix another precision:
                                       fast_ragged_dot (second formulation)
 * ``glu.*``                        -- SiLU-GLU forward/backward in float64 and
                                       as the float32 op sequence
+* ``unsort.unsort_bwd_rows``        -- weighted gradient and routing-weight row dot
 * ``bf16.*``                       -- bf16 rounding and ulp helpers
 
 Parity status: every function here is pinned by tests under ``tests/``
@@ -22,7 +23,7 @@ Parity status: every function here is pinned by tests under ``tests/``
 none is "parity unpinned".  The pages print no numeric input/output example,
 so no pin comes from printed values.
 """
-from . import bf16, glu, ragged  # noqa: F401
+from . import bf16, glu, ragged, unsort  # noqa: F401
 from .ragged import (  # noqa: F401
     group_bounds,
     ragged_dot,
