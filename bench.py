@@ -18,8 +18,8 @@ Also reported on the same line:
                 workload on this host's cores;
   ops           the other rows of the hot path at their own workloads
                 (packed GLU forward, dx, dw, decode pair in one CUDA graph,
-                standalone GLU forward/backward), each as time per call and
-                fraction of its roofline.
+                standalone GLU forward/backward, unsort backward), each as
+                time per call and fraction of its roofline.
 
 --impl reference times the oracle itself as the reference arm.
 Under torchrun (--gpus N) every rank runs an independent replica (no
@@ -267,6 +267,19 @@ def run_ops(rd, device, stream, peaks):
         Bb = w.limit * 1024 * 2 * 5
         res["glu_bwd"] = {"us": t * 1e6, "gbs": Bb / t / 1e9, "bound": "hbm", "frac": Bb / BW / t}
         del lhs, rhs, out, fused, gout, dfused
+        torch.cuda.empty_cache()
+
+        # valid-rows unsort backward at the packed buffer's shape [225280, 4096]
+        g = normal_bf16((w.m, 4096), 1.0, 33, device)
+        y = normal_bf16((w.m, 4096), 1.0, 34, device)
+        wt = torch.rand((w.m,), device=device)
+        grad = torch.empty_like(g)
+        dot = torch.empty((w.m,), dtype=torch.float32, device=device)
+        t = med(lambda: rd.unsort_bwd_rows(g, y, wt, lim, grad, dot))
+        Bu = w.limit * 4096 * 2 * 3 + w.limit * 8
+        res["unsort_bwd_rows"] = {"us": t * 1e6, "gbs": Bu / t / 1e9, "bound": "hbm",
+                                  "frac": Bu / BW / t}
+        del g, y, wt, grad, dot
         torch.cuda.empty_cache()
 
         # backward pair: dx and dw
@@ -542,6 +555,15 @@ def run_profile(args):
             x = normal_bf16((w.m, w.k), 1.0, 40, device)
             dw = torch.empty((w.g_total, w.k, w.n), dtype=torch.bfloat16, device=device)
             fn = lambda: rd.trans_ragged_dot(x, do, gs, out=dw)
+    elif name == "unsort":
+        w = workloads.packed_glu_fwd()
+        lim = torch.tensor([w.limit], dtype=torch.int32, device=device)
+        g = normal_bf16((w.m, 4096), 1.0, 33, device)
+        y = normal_bf16((w.m, 4096), 1.0, 34, device)
+        wt = torch.rand((w.m,), device=device)
+        grad = torch.empty_like(g)
+        dot = torch.empty((w.m,), dtype=torch.float32, device=device)
+        fn = lambda: rd.unsort_bwd_rows(g, y, wt, lim, grad, dot)
     elif name in ("glu_fwd", "glu_bwd"):
         w = workloads.packed_glu_fwd()
         lim = torch.tensor([w.limit], dtype=torch.int32, device=device)

@@ -12,6 +12,7 @@ Functions (same names as the C ABI, without the ``rd_`` prefix):
 * ``trans_ragged_dot(x, y, group_sizes, ...)``           -> out [g_local, k, n]
 * ``glu_fwd(fused, limit=None)``                         -> out [rows, f]
 * ``glu_bwd(fused, d_out, limit=None)``                  -> d_fused [rows, 2f]
+* ``unsort_bwd_rows(g, y, w, limit=None)``                -> (grad [rows, hidden], dot [rows])
 """
 from __future__ import annotations
 
@@ -21,7 +22,7 @@ from typing import Optional
 
 __all__ = [
     "load", "lib_path", "ragged_dot", "ragged_dot_trans_rhs", "trans_ragged_dot",
-    "glu_fwd", "glu_bwd", "RdError", "EPI_NONE", "EPI_SILU_GLU",
+    "glu_fwd", "glu_bwd", "unsort_bwd_rows", "RdError", "EPI_NONE", "EPI_SILU_GLU",
     "STATUS_NEG_SIZE", "STATUS_OVERFLOW", "STATUS_TIMEOUT", "MAX_GROUPS",
 ]
 
@@ -64,8 +65,9 @@ def load():
     lib.rd_trans_ragged_dot.argtypes = grouped + [ip, vp]
     lib.rd_glu_fwd.argtypes = [vp, vp, i64, i64, ip, vp]
     lib.rd_glu_bwd.argtypes = [vp, vp, vp, i64, i64, ip, vp]
+    lib.rd_unsort_bwd_rows.argtypes = [vp, vp, vp, vp, vp, i64, i64, ip, vp]
     for fn in (lib.rd_ragged_dot, lib.rd_ragged_dot_trans_rhs, lib.rd_trans_ragged_dot,
-               lib.rd_glu_fwd, lib.rd_glu_bwd):
+               lib.rd_glu_fwd, lib.rd_glu_bwd, lib.rd_unsort_bwd_rows):
         fn.restype = ctypes.c_int
     lib.rd_status_string.argtypes = [ctypes.c_int]
     lib.rd_status_string.restype = ctypes.c_char_p
@@ -211,3 +213,25 @@ def glu_bwd(fused, d_out, limit=None, out=None, stream=None):
                           _stream(stream))
     _check(code, "rd_glu_bwd")
     return out
+
+
+def unsort_bwd_rows(g, y, w, limit=None, grad=None, dot=None, stream=None):
+    """Weighted gradient bf16(f32(g) * w) and f32 row dot sum(g * y) over rows below limit."""
+    import torch
+
+    lib = load()
+    _bf16_2d(g, "g")
+    _bf16_2d(y, "y")
+    rows, hidden = g.shape
+    if y.shape != g.shape:
+        raise ValueError("g and y must have the same shape")
+    if w.dtype != torch.float32 or w.shape != (rows,) or not w.is_cuda:
+        raise ValueError("w must be a [rows] float32 CUDA tensor")
+    if grad is None:
+        grad = torch.empty_like(g)
+    if dot is None:
+        dot = torch.empty((rows,), dtype=torch.float32, device=g.device)
+    code = lib.rd_unsort_bwd_rows(_ptr(g), _ptr(y), _ptr(w), _ptr(grad), _ptr(dot), rows, hidden,
+                                  _ptr(limit), _stream(stream))
+    _check(code, "rd_unsort_bwd_rows")
+    return grad, dot

@@ -20,7 +20,7 @@ LIBDIR = os.path.join(PKG, "_lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIB = os.path.join(LIBDIR, "librd.so")
 
-SOURCES = ["api.cu", "gemm_fwd.cu", "gemm_dx.cu", "gemm_dw.cu", "glu.cu"]
+SOURCES = ["api.cu", "gemm_fwd.cu", "gemm_dx.cu", "gemm_dw.cu", "glu.cu", "unsort.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O3",
                  "-I" + os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]

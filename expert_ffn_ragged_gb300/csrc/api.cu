@@ -16,7 +16,18 @@
 namespace rd {
 namespace {
 
-constexpr uint64_t kTimeoutNs = 4000000000ull;  // bound of any single wait inside a kernel
+constexpr uint64_t kTimeoutNs = 4000000000ull;  // default bound of any single wait in a kernel
+
+// Bound of each wait inside the grouped-GEMM kernels: RD_WAIT_TIMEOUT_NS when
+// set (read at every call; a test uses a tiny value to drive the timeout and
+// unwind path), else 4 s.
+uint64_t wait_timeout_ns() {
+  const char* v = getenv("RD_WAIT_TIMEOUT_NS");
+  if (v == nullptr || *v == 0) return kTimeoutNs;
+  char* end = nullptr;
+  const unsigned long long t = strtoull(v, &end, 10);
+  return (end != nullptr && *end == 0) ? static_cast<uint64_t>(t) : kTimeoutNs;
+}
 constexpr int64_t kMaxDim = 0x7FFFFFFF;
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -197,7 +208,7 @@ extern "C" rd_status rd_ragged_dot(const void* lhs, const void* rhs, void* out, 
   const int tile_w = glu ? kBN / 2 : kBN;
   a.n_tiles = static_cast<int32_t>((n_out + tile_w - 1) / tile_w);
   a.dw_m_tiles = 0;
-  a.timeout_ns = kTimeoutNs;
+  a.timeout_ns = wait_timeout_ns();
   const bool pair = use_pair(sms, m, g_total);
   const int grid = pair ? pair_grid(sms, ((m + 2 * kBM - 1) / (2 * kBM) + g_local) * a.n_tiles)
                         : grid_for(sms, ((m + kBM - 1) / kBM + g_local) * a.n_tiles);
@@ -253,7 +264,7 @@ extern "C" rd_status rd_ragged_dot_trans_rhs(const void* lhs, const void* rhs, v
   a.group_offset = group_offset;
   a.g_local = g_local;
   a.n_tiles = static_cast<int32_t>((k + kBN - 1) / kBN);
-  a.timeout_ns = kTimeoutNs;
+  a.timeout_ns = wait_timeout_ns();
   const int grid = pair ? pair_grid(sms, ((m + 2 * kBM - 1) / (2 * kBM) + g_local) * a.n_tiles)
                         : grid_for(sms, ((m + kBM - 1) / kBM + g_local) * a.n_tiles);
   return launch_gemm_dx(pair, ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) ==
@@ -292,6 +303,8 @@ extern "C" rd_status rd_trans_ragged_dot(const void* x, const void* y, void* out
     const uint32_t bb[2] = {64, kBK};
     if ((st = encode(&tb, y, 2, db, sb, bb)) != RD_OK) return st;
   }
+  const bool pair = use_pair(sms, m, g_total);
+  const int tile_rows = pair ? 2 * kBM : kBM;  // rows of dw[j] (the k axis) per tile
   GemmArgs a = {};
   a.group_sizes = group_sizes;
   a.limit = limit;
@@ -305,12 +318,13 @@ extern "C" rd_status rd_trans_ragged_dot(const void* x, const void* y, void* out
   a.group_offset = group_offset;
   a.g_local = g_local;
   a.n_tiles = static_cast<int32_t>((n + kBN - 1) / kBN);
-  a.dw_m_tiles = static_cast<int32_t>((k + kBM - 1) / kBM);
-  a.timeout_ns = kTimeoutNs;
+  a.dw_m_tiles = static_cast<int32_t>((k + tile_rows - 1) / tile_rows);
+  a.timeout_ns = wait_timeout_ns();
   const int64_t tiles = static_cast<int64_t>(g_local) * a.dw_m_tiles * a.n_tiles;
   if (tiles > kMaxDim) return RD_ERR_UNSUPPORTED;
-  const int grid = grid_for(sms, tiles);
-  return launch_gemm_dw(ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+  const int grid = pair ? pair_grid(sms, tiles) : grid_for(sms, tiles);
+  return launch_gemm_dw(pair, ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
              ? RD_OK
              : RD_ERR_CUDA;
 }
@@ -364,6 +378,36 @@ extern "C" rd_status rd_glu_bwd(const void* fused, const void* d_out, void* d_fu
   return launch_glu_bwd(fused, d_out, d_fused, static_cast<int32_t>(rows),
                         static_cast<int32_t>(f), limit, grid,
                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RD_OK
+             : RD_ERR_CUDA;
+}
+
+extern "C" rd_status rd_unsort_bwd_rows(const void* g, const void* y, const float* w, void* grad,
+                                        float* dot, int64_t rows, int64_t hidden,
+                                        const int32_t* limit, rd_stream_t stream) {
+  if (rows < 0 || hidden < 0) return RD_ERR_INVALID_ARG;
+  if (rows > kMaxDim || hidden > kMaxDim) return RD_ERR_UNSUPPORTED;
+  if (hidden % 8 != 0) return RD_ERR_UNSUPPORTED;
+  if (rows > 0 && (w == nullptr || dot == nullptr)) return RD_ERR_INVALID_ARG;
+  if (rows > 0 && hidden > 0 && (g == nullptr || y == nullptr || grad == nullptr))
+    return RD_ERR_INVALID_ARG;
+  if (!aligned16(g) || !aligned16(y) || !aligned16(grad) ||
+      (reinterpret_cast<uintptr_t>(w) & 3u) || (reinterpret_cast<uintptr_t>(dot) & 3u) ||
+      (reinterpret_cast<uintptr_t>(limit) & 3u))
+    return RD_ERR_UNSUPPORTED;
+  const uint64_t mb = static_cast<uint64_t>(rows) * hidden * 2, rb = static_cast<uint64_t>(rows) * 4;
+  if (overlap(grad, mb, g, mb) || overlap(grad, mb, y, mb) || overlap(grad, mb, w, rb) ||
+      overlap(grad, mb, dot, rb) || overlap(grad, mb, limit, 4) || overlap(dot, rb, g, mb) ||
+      overlap(dot, rb, y, mb) || overlap(dot, rb, w, rb) || overlap(dot, rb, limit, 4))
+    return RD_ERR_INVALID_ARG;
+  rd_status st;
+  int sms = 0;
+  if ((st = current_device(&sms)) != RD_OK) return st;
+  if (rows == 0) return RD_OK;
+  const int grid = grid_for(sms * 8, (rows + 7) / 8);
+  return launch_unsort_bwd_rows(g, y, w, grad, dot, static_cast<int32_t>(rows),
+                                static_cast<int32_t>(hidden), limit, grid,
+                                reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? RD_OK
              : RD_ERR_CUDA;
 }

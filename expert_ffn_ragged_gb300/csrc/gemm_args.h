@@ -48,12 +48,16 @@ cudaError_t launch_gemm_fwd(bool glu, bool pair, const CUtensorMap& tmap_a,
                             cudaStream_t stream);
 cudaError_t launch_gemm_dx(bool pair, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                            const GemmArgs& args, int grid, cudaStream_t stream);
-cudaError_t launch_gemm_dw(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+cudaError_t launch_gemm_dw(bool pair, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                            const GemmArgs& args, int grid, cudaStream_t stream);
 
 cudaError_t launch_glu_fwd(const void* fused, void* out, int32_t rows, int32_t f,
                            const int32_t* limit, int grid, cudaStream_t stream);
 cudaError_t launch_glu_bwd(const void* fused, const void* d_out, void* d_fused, int32_t rows,
                            int32_t f, const int32_t* limit, int grid, cudaStream_t stream);
+
+cudaError_t launch_unsort_bwd_rows(const void* g, const void* y, const float* w, void* grad,
+                                   float* dot, int32_t rows, int32_t hidden, const int32_t* limit,
+                                   int grid, cudaStream_t stream);
 
 }  // namespace rd

@@ -15,13 +15,15 @@
 //   * every CTA reads group_sizes and *limit itself and builds the group
 //     boundaries (exclusive prefix clamped to L) and the per-group tile
 //     prefix in shared memory -- no workspace, no host round trip;
-//   * tiles are handed out by static striding over (group, m-tile, n-tile)
-//     with m fastest, so the CTAs working at one time share each rhs column
-//     panel through L2;
+//   * tiles are handed out by static striding over (group, band, n-tile,
+//     m-tile): within a band of 4096 rows the m-tiles run fastest, so the CTAs
+//     working at one time share each rhs column panel through L2 and the
+//     band's lhs rows stay in L2 until every column panel has used them;
 //   * warp 0 (one lane) streams A/B blocks with TMA into a ring of
 //     128-byte-swizzled tiles; warp 1 issues tcgen05.mma into one of two
 //     TMEM accumulators; warps 2-5 drain the other accumulator with
-//     tcgen05.ld, round to bf16 (or apply the GLU) and store with row masks;
+//     tcgen05.ld, round to bf16 (or apply the GLU) and store full 64-byte row
+//     segments through a small shared-memory transpose, with row masks;
 //     warps 6-7 write the zero rows of the forward/dx outputs;
 //   * PAIR=false: one CTA per SM computes a 128x256 tile (UMMA 128x256x16,
 //     4-stage ring of 48 KB).  PAIR=true: a cluster of two CTAs computes a
@@ -50,6 +52,13 @@
 
 namespace rd {
 
+// Bounds of the waits made while unwinding after a timeout: every copy or MMA
+// still in flight then completes within microseconds.
+constexpr uint64_t kDrainNs = 1000000000ull;
+constexpr uint64_t kGraceNs = 200000ull;
+// rows of lhs kept hot in L2 while a band of tiles sweeps the output columns
+constexpr int kBandRows = 4096;
+
 template <bool PAIR>
 struct TileCfg {
   static constexpr int kStagesN = PAIR ? 6 : 4;
@@ -65,6 +74,7 @@ struct alignas(16) GemmShared {
   static constexpr int S = TileCfg<PAIR>::kStagesN;
   uint64_t full[S];
   uint64_t empty[S];
+  uint64_t pready[S];  // pair dw: the odd CTA's zeroed edge block is ready
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -76,6 +86,7 @@ struct alignas(16) GemmShared {
   int32_t zero_hi;  // forward/dx: rows [zero_hi, L) are zero
   int32_t bound[kMaxGroups + 1];       // group boundaries, clamped to L
   int32_t tile_start[kMaxGroups + 1];  // first tile of each local group
+  uint4 epi[4][32 * 4];                // epilogue staging: 32 rows x 64 bytes per warp
 };
 
 template <bool PAIR>
@@ -193,9 +204,16 @@ __device__ __forceinline__ Tile decode_tile(const GemmShared<PAIR>& sh, const Ge
     const int u = t - sh.tile_start[lo];
     tl.rs = sh.bound[a.group_offset + lo];
     tl.re = sh.bound[a.group_offset + lo + 1];
+    // Bands of kBandRows rows: within a band the m-tiles run fastest and the
+    // band sweeps every n-tile before the next band starts, so the band's lhs
+    // rows stay in L2 while each rhs column panel is read once per band.
+    constexpr int kBand = kBandRows / TM;
     const int mt = (tl.re - tl.rs + TM - 1) / TM;
-    tl.m_idx = u % mt;
-    tl.n_idx = u / mt;
+    const int band = u / (kBand * a.n_tiles);
+    const int rem = u - band * kBand * a.n_tiles;
+    const int bw = min(kBand, mt - band * kBand);
+    tl.m_idx = band * kBand + rem % bw;
+    tl.n_idx = rem / bw;
     const int first = tl.rs + tl.m_idx * TM;
     tl.row_load = (tl.m_idx == mt - 1) ? tl.re - TM : first;
     tl.nkb = (a.kc + kBK - 1) / kBK;
@@ -203,16 +221,38 @@ __device__ __forceinline__ Tile decode_tile(const GemmShared<PAIR>& sh, const Ge
   return tl;
 }
 
-// Store 32 consecutive bf16 (packed in 16 words) of one row, masked per 8 columns.
-__device__ __forceinline__ void store_row32(__nv_bfloat16* row_ptr, int col, int n_out,
-                                            const uint32_t (&p)[16]) {
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    if (col + 8 * v + 8 <= n_out) {
-      *reinterpret_cast<uint4*>(row_ptr + col + 8 * v) =
-          make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
-    }
+// dw: rows of the last K block of a group that precede the block's own start
+// (the block is loaded from row end - 64).  Whole 16-row K steps of them are
+// skipped by the MMA; the rows of the step that straddles the start must be
+// zeroed in shared memory.  Returns the first K step to issue and sets
+// [z0, z1) to the rows to zero (empty when z0 == z1).
+__device__ __forceinline__ int dw_edge(const Tile& tl, int kb, int& z0, int& z1) {
+  z0 = z1 = 0;
+  if (kb != tl.nkb - 1) return 0;
+  const int rem = (tl.re - tl.rs) - (tl.nkb - 1) * kBK;
+  const int zrows = kBK - rem;
+  z0 = zrows & ~15;
+  z1 = zrows;
+  return zrows >> 4;
+}
+
+// Zero rows [z0, z1) of one stage of a dw block in both operands: each row is
+// one 128-byte line per 64-wide chunk (A chunks, then B chunks).  Then make
+// the writes visible to the tensor core (async proxy).
+template <int A_CHUNKS, int B_CHUNKS>
+__device__ __forceinline__ void dw_zero_rows(uint8_t* a_st, uint8_t* b_st, int z0, int z1, int lane) {
+  constexpr int kChunks = A_CHUNKS + B_CHUNKS;
+  const int nunits = (z1 - z0) * kChunks * 8;  // 16-byte units
+  for (int u = lane; u < nunits; u += 32) {
+    const int row = z0 + u / (kChunks * 8);
+    const int rest = u % (kChunks * 8);
+    const int chunk = rest >> 3;
+    const int part = rest & 7;
+    uint8_t* base = chunk < A_CHUNKS ? a_st + chunk * (kBK * 128)
+                                     : b_st + (chunk - A_CHUNKS) * (kBK * 128);
+    *reinterpret_cast<uint4*>(base + row * 128 + part * 16) = make_uint4(0, 0, 0, 0);
   }
+  ptx::fence_proxy_async_smem();
 }
 
 template <int OP, bool GLU, bool PAIR>
@@ -222,7 +262,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   using Cfg = TileCfg<PAIR>;
   constexpr int S = Cfg::kStagesN;
   constexpr int TM = Cfg::kTileM;
-  static_assert(!(PAIR && OP == kOpDw), "the pair variant covers the forward and dx");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -242,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(ptx::smem_addr(&sh.full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&sh.empty[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&sh.pready[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ptx::smem_addr(&sh.tfull[b]), 1);
@@ -292,7 +332,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb_local = ptx::smem_addr(&sh.full[stage]);
           const uint32_t a_dst = ptx::smem_addr(sA + stage * Cfg::kStageA);
           const uint32_t b_dst = ptx::smem_addr(sB + stage * Cfg::kStageB);
-          if (PAIR) {
+          if (PAIR && OP == kOpDw) {
+            // The last block of a group whose start straddles a 16-row K step is zeroed
+            // in each CTA before the MMA: the odd CTA's copy then counts on its own
+            // barrier (its warp 1 zeroes and signals), the even CTA expects only its own.
+            int z0, z1;
+            dw_edge(tl, kb, z0, z1);
+            const bool edge = z1 > z0;
+            const uint32_t fb = edge ? fb_local : ptx::map_to_rank(fb_local, 0);
+            if (rank == 0 || edge)
+              ptx::mbar_arrive_expect_tx(fb_local, (edge ? 1 : 2) * Cfg::kStageBytes);
+            const int row0 = (kb == tl.nkb - 1) ? tl.re - kBK : tl.rs + kb * kBK;
+            const int ka = tl.m_idx * TM + static_cast<int>(rank) * kBM;
+            const int nb = tl.n_idx * kBN + static_cast<int>(rank) * (kBN / 2);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              ptx::tma_load_2d_pair(a_dst + c * (kBK * 128), &tmap_a, fb, ka + c * 64, row0);
+              ptx::tma_load_2d_pair(b_dst + c * (kBK * 128), &tmap_b, fb, nb + c * 64, row0);
+            }
+          } else if (PAIR) {
             // Both CTAs' bytes are counted on the even CTA's barrier, which expects them
             // all; the odd CTA's copies may land before that expectation is posted (the
             // phase cannot complete before the even CTA's arrival).
@@ -345,17 +403,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Wait until every fill of this CTA's ring has been consumed, so that no MMA
       // commit (possibly from the peer CTA) arrives on a barrier after this CTA exits.
-      // On abort, wait (bounded) for the copies still in flight instead.
+      // On abort, wait (bounded) for the copies still in flight instead; the odd CTA
+      // of a pair cannot observe its copies (they count on the even CTA's barrier),
+      // so it gives them a fixed grace period.
       volatile int no_abort = 0;
       for (int s = 0; s < S; ++s) {
         if (!(pend_mask & (1u << s))) continue;
         const uint32_t par = (pend_par >> s) & 1u;
         if (*abort_flag) {
           if (!PAIR || rank == 0)
-            ptx::mbar_wait_bounded(ptx::smem_addr(&sh.full[s]), par, &no_abort, tlimit);
+            ptx::mbar_wait_bounded(ptx::smem_addr(&sh.full[s]), par, &no_abort, kDrainNs);
         } else {
-          ptx::mbar_wait_bounded(ptx::smem_addr(&sh.empty[s]), par, &no_abort, tlimit);
+          ptx::mbar_wait_bounded(ptx::smem_addr(&sh.empty[s]), par, &no_abort, kDrainNs);
         }
+      }
+      if (PAIR && rank != 0 && *abort_flag && pend_mask != 0) {
+        const uint64_t t0 = ptx::global_timer_ns();
+        while (ptx::global_timer_ns() - t0 < kGraceNs) __nanosleep(1000);
       }
     }
   } else if (warp == 1) {
@@ -369,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      uint32_t pready_par = 0;
       bool ok = true;
       for (int t = unit; t < total && ok; t += units) {
         const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
@@ -388,30 +453,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* a_st = sA + stage * Cfg::kStageA;
           uint8_t* b_st = sB + stage * Cfg::kStageB;
           int kk0 = 0;  // first 16-deep K step issued for this block
-          if (OP == kOpDw && kb == tl.nkb - 1) {
-            // The last block was loaded from row (end - 64); its first zrows rows precede
-            // the block's own start.  Whole 16-row K steps of them are skipped; the rows of
-            // the straddling step are zeroed in both operands so nothing from a
-            // neighbouring group (or a NaN) enters the sum.
-            const int rem = (tl.re - tl.rs) - (tl.nkb - 1) * kBK;
-            const int zrows = kBK - rem;
-            kk0 = zrows >> 4;
-            const int z0 = kk0 << 4;
-            if (zrows > z0) {
-              // each row is one 128-byte line per 64-wide chunk: 2 chunks of A, 4 of B
-              const int nunits = (zrows - z0) * 6 * 8;  // 16-byte units
-              for (int u = lane; u < nunits; u += 32) {
-                const int row = z0 + u / 48;
-                const int rest = u % 48;
-                const int chunk = rest >> 3;
-                const int part = rest & 7;
-                uint8_t* base = chunk < 2 ? a_st + chunk * (kBK * 128)
-                                          : b_st + (chunk - 2) * (kBK * 128);
-                *reinterpret_cast<uint4*>(base + row * 128 + part * 16) = make_uint4(0, 0, 0, 0);
+          if (OP == kOpDw) {
+            // rows of a neighbouring group (or a NaN) must not enter the sum
+            int z0, z1;
+            kk0 = dw_edge(tl, kb, z0, z1);
+            if (z1 > z0) {
+              dw_zero_rows<2, Cfg::kBCols / 64>(a_st, b_st, z0, z1, lane);
+              __syncwarp();
+              if (PAIR) {
+                // the odd CTA has zeroed the same rows of its half
+                ok = ptx::mbar_wait_bounded_cluster(ptx::smem_addr(&sh.pready[stage]),
+                                                    (pready_par >> stage) & 1u, abort_flag, tlimit);
+                pready_par ^= 1u << stage;
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                if (!ok) break;
               }
-              ptx::fence_proxy_async_smem();
             }
-            __syncwarp();
           }
           if (lane == 0) {
             const uint32_t a_addr = ptx::smem_addr(a_st);
@@ -451,45 +508,90 @@ __global__ void __launch_bounds__(kThreads, 1)
           volatile int no_abort = 0;
           if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&sh.drain), 0x1);
           else ptx::tc_commit(ptx::smem_addr(&sh.drain));
-          ptx::mbar_wait_bounded(ptx::smem_addr(&sh.drain), 0, &no_abort, tlimit);
+          ptx::mbar_wait_bounded(ptx::smem_addr(&sh.drain), 0, &no_abort, kDrainNs);
         }
         __syncwarp();
+      }
+    } else if (OP == kOpDw) {
+      // odd CTA of a dw pair: zero the straddling rows of each edge block once its own
+      // copy has landed, then tell the even CTA, whose MMA reads this CTA's half
+      int stage = 0;
+      uint32_t lpar = 0;  // phase of this CTA's own full barrier, per stage
+      const uint32_t pready0 = ptx::map_to_rank(ptx::smem_addr(&sh.pready[0]), 0);
+      bool ok = true;
+      for (int t = unit; t < total && ok; t += units) {
+        const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
+        for (int kb = 0; kb < tl.nkb; ++kb) {
+          int z0, z1;
+          dw_edge(tl, kb, z0, z1);
+          if (z1 > z0) {
+            ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.full[stage]), (lpar >> stage) & 1u,
+                                        abort_flag, tlimit);
+            lpar ^= 1u << stage;
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            if (!ok) break;
+            dw_zero_rows<2, Cfg::kBCols / 64>(sA + stage * Cfg::kStageA, sB + stage * Cfg::kStageB,
+                                             z0, z1, lane);
+            __syncwarp();
+            if (lane == 0)
+              ptx::mbar_arrive_cluster(pready0 + static_cast<uint32_t>(stage * sizeof(uint64_t)));
+          }
+          if (++stage == S) stage = 0;
+        }
       }
     }
   } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
+    // Each warp owns one 32-lane quarter of the accumulator (32 tile rows).  A
+    // 32-column chunk is read from TMEM (thread = row), rounded to bf16 (or
+    // put through the GLU), transposed through a 2 KB XOR-swizzled staging
+    // buffer, and stored 8 rows x 64 contiguous bytes per instruction.
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int r_in_tile = static_cast<int>(rank) * kBM + q * 32 + lane;
     constexpr int tile_w = GLU ? kBN / 2 : kBN;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
+    uint4* stg = sh.epi[q];
     const uint32_t tempty_leader =
         PAIR ? ptx::map_to_rank(ptx::smem_addr(&sh.tempty[0]), 0) : 0u;
+    const int sr = lane >> 2;      // row (within 8) this lane stores
+    const int piece = lane & 3;    // 16-byte piece of the row's 64 bytes
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = unit; t < total; t += units) {
       const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
-      // destination row of this thread and whether it owns it
-      int row;
-      bool valid;
-      __nv_bfloat16* row_ptr;
-      if (OP == kOpDw) {
-        row = tl.m_idx * kBM + r_in_tile;
-        valid = row < args.m_out;
-        row_ptr = out + (static_cast<size_t>(tl.j) * args.m_out + row) * args.n_out;
-      } else {
-        row = tl.row_load + r_in_tile;
-        valid = row >= tl.rs + tl.m_idx * TM && row < tl.re;
-        row_ptr = out + static_cast<size_t>(row) * args.n_out;
-      }
+      // first row of this warp's 32 rows and the rows it may write: [lo, hi)
+      const int wrow0 = (OP == kOpDw ? tl.m_idx * TM : tl.row_load) +
+                        static_cast<int>(rank) * kBM + q * 32;
+      const int lo = OP == kOpDw ? 0 : tl.rs + tl.m_idx * TM;
+      const int hi = OP == kOpDw ? args.m_out : tl.re;
+      __nv_bfloat16* base =
+          OP == kOpDw ? out + static_cast<size_t>(tl.j) * args.m_out * args.n_out : out;
       const int col0 = tl.n_idx * tile_w;
+      // write the 16 packed words of this lane's row into the staging buffer, then
+      // store the chunk's 32 rows x 32 columns to global memory
+      auto emit = [&](const uint32_t (&p)[16], int col) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          stg[lane * 4 + (v ^ ((lane >> 1) & 3))] =
+              make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          const int rl = it * 8 + sr;
+          const uint4 val = stg[rl * 4 + (piece ^ ((rl >> 1) & 3))];
+          const int row = wrow0 + rl;
+          const int c = col + piece * 8;
+          if (row >= lo && row < hi && c + 8 <= args.n_out)
+            *reinterpret_cast<uint4*>(base + static_cast<size_t>(row) * args.n_out + c) = val;
+        }
+        __syncwarp();
+      };
       if (tl.nkb == 0) {
         const uint32_t z[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
-        if (valid)
-          for (int c = 0; c < tile_w / 32; ++c) store_row32(row_ptr, col0 + c * 32, args.n_out, z);
+        for (int c = 0; c < tile_w / 32; ++c) emit(z, col0 + c * 32);
         continue;
       }
-      bool ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.tfull[acc]), acc_phase,
-                                               abort_flag, tlimit);
+      bool ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.tfull[acc]), acc_phase, abort_flag,
+                                       tlimit);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
       ptx::tc_fence_after();
@@ -506,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p[i] = pack_bf16x2(glu_fwd_f32(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
                                glu_fwd_f32(__uint_as_float(g[2 * i + 1]),
                                            __uint_as_float(u[2 * i + 1])));
-          if (valid) store_row32(row_ptr, col0 + c * 32, args.n_out, p);
+          emit(p, col0 + c * 32);
         }
       } else {
 #pragma unroll 1
@@ -516,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             p[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          if (valid) store_row32(row_ptr, col0 + c * 32, args.n_out, p);
+          emit(p, col0 + c * 32);
         }
       }
       ptx::tc_fence_before();

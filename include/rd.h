@@ -31,6 +31,13 @@
  * summing past m, a bounded wait that ran out) never traps: the kernel
  * clamps and, when `status` is not NULL, ORs an RD_STATUS_* bit into
  * *status.  The library never clears *status.
+ *
+ * Bounded waits: every wait inside the grouped-GEMM kernels gives up after
+ * 4 s (or the number of nanoseconds in the environment variable
+ * RD_WAIT_TIMEOUT_NS, read at each call).  A kernel that gives up finishes
+ * its copies and MMAs in flight, frees its tensor memory, returns, and sets
+ * RD_STATUS_TIMEOUT; its outputs are then incomplete but the CUDA context
+ * stays usable.
  */
 #ifndef RD_H_
 #define RD_H_
@@ -156,6 +163,26 @@ rd_status rd_glu_fwd(const void* fused, void* out, int64_t rows, int64_t f,
  */
 rd_status rd_glu_bwd(const void* fused, const void* d_out, void* d_fused, int64_t rows,
                      int64_t f, const int32_t* limit, rd_stream_t stream);
+
+/*
+ * rd_unsort_bwd_rows -- valid-rows unsort backward.
+ *   grad[r, :] = bf16( f32(g[r, :]) * w[r] )               (one f32 multiply, one rounding)
+ *   dot[r]     = sum_c f32(g[r, c]) * f32(y[r, c])         (f32 accumulation)
+ *   for r < L; rows >= L of grad and dot are not written, of g, y, w not read.
+ * Defined by MaxText PR #5760 (commit message, kernels/ragged/unsort_bwd_rows.py:
+ * the weighted gradient and the f32 routing-weight row dot over rows < limit;
+ * review comment: the per-row dot must not be assembled by concurrent blocks).
+ * Each row is owned by one warp, so the result has no cross-CTA race.
+ *
+ *   g [rows, hidden] bf16 (gathered gradient), y [rows, hidden] bf16 (sorted
+ *   tokens), w [rows] f32 (routing weights), grad [rows, hidden] bf16,
+ *   dot [rows] f32, limit device int32 or NULL.
+ * Requires hidden % 8 == 0, 16-byte aligned bf16 pointers, 4-byte aligned
+ * w and dot; grad and dot must not overlap the inputs.
+ */
+rd_status rd_unsort_bwd_rows(const void* g, const void* y, const float* w, void* grad, float* dot,
+                             int64_t rows, int64_t hidden, const int32_t* limit,
+                             rd_stream_t stream);
 
 /* A static, human-readable name for a status code. */
 const char* rd_status_string(rd_status s);

@@ -30,7 +30,7 @@ def _declared():
 def test_header_declares_the_abi():
     assert _declared() == sorted([
         "rd_glu_bwd", "rd_glu_fwd", "rd_ragged_dot", "rd_ragged_dot_trans_rhs",
-        "rd_status_string", "rd_trans_ragged_dot"])
+        "rd_status_string", "rd_trans_ragged_dot", "rd_unsort_bwd_rows"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -102,3 +102,9 @@ def test_other_entry_points_check_arguments(lib):
     lib.rd_glu_bwd.argtypes = [v, v, v, i64, i64, v, v]
     assert lib.rd_glu_bwd(P, P * 0x100, P, 16, 16, None, None) == RD_ERR_INVALID_ARG
     assert lib.rd_glu_bwd(P, P * 0x100, P * 0x10000, -1, 16, None, None) == RD_ERR_INVALID_ARG
+    f = lib.rd_unsort_bwd_rows
+    f.restype = ctypes.c_int
+    f.argtypes = [v, v, v, v, v, i64, i64, v, v]
+    assert f(P, P * 0x100, P * 0x200, P * 0x10000, P * 0x20000, 16, 12, None, None) == RD_ERR_UNSUPPORTED
+    assert f(P, P * 0x100, None, P * 0x10000, P * 0x20000, 16, 16, None, None) == RD_ERR_INVALID_ARG
+    assert f(P, P * 0x100, P * 0x200, P, P * 0x20000, 16, 16, None, None) == RD_ERR_INVALID_ARG
