@@ -10,6 +10,8 @@ float64 unless the pages fix another precision:
 
 * ``ragged.ragged_dot``            -- grouped forward with group_offset and limit
 * ``ragged.ragged_dot_trans_rhs``  -- the trans_rhs form used for dx
+* ``ragged.ragged_dot_trans_rhs_glu_bwd`` -- dx of the down projection followed
+                                      by the SiLU-GLU backward
 * ``ragged.trans_ragged_dot``      -- per-group weight gradient x^T y
 * ``ragged.ragged_dot_adjusted``   -- the boundary-absorbing formulation of
                                       fast_ragged_dot (second formulation)
@@ -29,6 +31,7 @@ from .ragged import (  # noqa: F401
     ragged_dot,
     ragged_dot_adjusted,
     ragged_dot_trans_rhs,
+    ragged_dot_trans_rhs_glu_bwd,
     trans_ragged_dot,
 )
 from .glu import (  # noqa: F401

@@ -28,7 +28,7 @@ from typing import Optional
 
 import numpy as np
 
-from .glu import glu_fwd_f64
+from .glu import glu_bwd_f64, glu_fwd_f64
 
 
 def group_bounds(group_sizes, m: int, limit: Optional[int] = None):
@@ -158,3 +158,32 @@ def ragged_dot_adjusted(lhs, rhs, group_sizes, group_offset: int = 0) -> np.ndar
     rows = np.arange(m)
     valid = (rows >= shard_start) & (rows < shard_end)
     return np.where(valid[:, None], full, 0.0)
+
+
+def ragged_dot_trans_rhs_glu_bwd(d_out, rhs, fused, group_sizes, group_offset: int = 0,
+                                 limit: Optional[int] = None):
+    """SiLU-GLU backward of an expert FFN, through its down projection.
+
+    Forward of the layer (per local group j): h = silu(gate) * up with
+    [gate | up] = fused [m, 2f], then out = h @ rhs[j] with rhs [g_local, f, n].
+    Given the output gradient d_out [m, n]: dh = d_out @ rhs[j]^T (the
+    trans_rhs form, SkyRL PR #867 backward fix) and the GLU backward of
+    MaxText PR #5760 (commit message: [d_gate | d_up] in one pass, recomputing
+    the forward from the saved fused buffer).  Returns float64 [m, 2f]:
+    [d_gate | d_up] on local rows, 0 on the other rows below L, NaN at or past L.
+    """
+    a = np.asarray(d_out, dtype=np.float64)
+    fz = np.asarray(fused, dtype=np.float64)
+    m, f2 = fz.shape
+    f = f2 // 2
+    dh = ragged_dot_trans_rhs(a, rhs, group_sizes, group_offset, limit)
+    b, L = group_bounds(group_sizes, m, limit)
+    g_local = np.asarray(rhs).shape[0]
+    out = np.full((m, 2 * f), np.nan)
+    out[:L] = 0.0
+    lo, hi = b[group_offset], b[group_offset + g_local]
+    if hi > lo:
+        d_gate, d_up = glu_bwd_f64(fz[lo:hi, :f], fz[lo:hi, f:], dh[lo:hi])
+        out[lo:hi, :f] = d_gate
+        out[lo:hi, f:] = d_up
+    return out

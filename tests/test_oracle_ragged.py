@@ -373,3 +373,41 @@ def test_planted_dropped_term_is_caught():
     good = brute_fwd(lhs.tolist(), rhs.tolist(), sizes.tolist(), 0, None)
     dropped = oracle.ragged_dot(lhs[:, :2], rhs[:, :2], sizes)   # last k term dropped
     assert not np.allclose(good, dropped)
+
+
+# --------------------------------------------------------------------------
+# the GLU backward through the down projection
+# --------------------------------------------------------------------------
+def _ffn_loss(fused, w_down, d_out, sizes, off, limit):
+    """<ragged_dot(glu(gate, up), w_down), d_out> over the local rows below L."""
+    m, f2 = fused.shape
+    f = f2 // 2
+    h = oracle.glu_fwd_f64(fused[:, :f], fused[:, f:])
+    out = oracle.ragged_dot(h, w_down, sizes, group_offset=off, limit=limit)
+    b, L = oracle.group_bounds(sizes, m, limit)
+    rows = slice(b[off], b[off + w_down.shape[0]])
+    return float(np.sum(out[rows] * d_out[rows]))
+
+
+def test_glu_bwd_through_down_projection_matches_finite_differences():
+    rng = np.random.default_rng(21)
+    m, f, n, g = 24, 4, 5, 3
+    sizes = [7, 9, 8]
+    fused = rng.standard_normal((m, 2 * f))
+    w_down = rng.standard_normal((g, f, n))        # forward: h [m, f] @ w_down[j] [f, n]
+    d_out = rng.standard_normal((m, n))
+    for off, gl, limit in [(0, 3, None), (1, 2, 20)]:
+        wl = w_down[off:off + gl]
+        grad = oracle.ragged_dot_trans_rhs_glu_bwd(d_out, wl, fused, sizes, off, limit)
+        b, L = oracle.group_bounds(sizes, m, limit)
+        h = 1e-6
+        for _ in range(12):
+            i, c = int(rng.integers(0, m)), int(rng.integers(0, 2 * f))
+            fp, fm = fused.copy(), fused.copy()
+            fp[i, c] += h
+            fm[i, c] -= h
+            fd = (_ffn_loss(fp, wl, d_out, sizes, off, limit) - _ffn_loss(fm, wl, d_out, sizes, off, limit)) / (2 * h)
+            if i < L:
+                assert math.isclose(grad[i, c], fd, rel_tol=1e-6, abs_tol=1e-8), (i, c)
+            else:
+                assert np.isnan(grad[i, c]) and fd == 0.0
