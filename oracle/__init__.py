@@ -13,6 +13,7 @@ float64 unless the pages fix another precision:
 * ``ragged.ragged_dot_trans_rhs_glu_bwd`` -- dx of the down projection followed
                                       by the SiLU-GLU backward
 * ``ragged.trans_ragged_dot``      -- per-group weight gradient x^T y
+* ``ragged.trans_ragged_dot_f32``  -- the same in f32, optionally accumulated
 * ``ragged.ragged_dot_adjusted``   -- the boundary-absorbing formulation of
                                       fast_ragged_dot (second formulation)
 * ``glu.*``                        -- SiLU-GLU forward/backward in float64 and
@@ -33,6 +34,7 @@ from .ragged import (  # noqa: F401
     ragged_dot_trans_rhs,
     ragged_dot_trans_rhs_glu_bwd,
     trans_ragged_dot,
+    trans_ragged_dot_f32,
 )
 from .glu import (  # noqa: F401
     glu_bwd_f32,

@@ -187,3 +187,46 @@ def ragged_dot_trans_rhs_glu_bwd(d_out, rhs, fused, group_sizes, group_offset: i
         out[lo:hi, :f] = d_gate
         out[lo:hi, f:] = d_up
     return out
+
+
+def trans_ragged_dot_f32(x, y, group_sizes, group_offset: int = 0, g_local: Optional[int] = None,
+                         limit: Optional[int] = None, out_prior=None) -> np.ndarray:
+    """trans_ragged_dot kept in f32 precision, optionally accumulated into a prior buffer.
+
+    The page's _gpu_trans_ragged_dot_fwd takes ``acc_dtype`` (f32) separately
+    from the compute dtype (SkyRL PR #867); keeping the f32 result, and adding
+    it to an existing gradient buffer, is the accumulation a training step does
+    across micro-batches.  Returns float64: ``out_prior + x^T y`` per local
+    group (``out_prior`` = 0 when absent); a group without rows leaves its
+    prior block unchanged.
+    """
+    d = trans_ragged_dot(x, y, group_sizes, group_offset, g_local, limit)
+    if out_prior is None:
+        return d
+    prior = np.asarray(out_prior, dtype=np.float64)
+    assert prior.shape == d.shape
+    return prior + d
+
+
+def f32_sum_bound(x, y, group_sizes, group_offset: int = 0, g_local: Optional[int] = None,
+                  limit: Optional[int] = None) -> np.ndarray:
+    """Worst-case error of an f32 accumulation of the exact products, any order.
+
+    Each product of two bf16 values is exact in f32; a sum of kc such terms
+    in f32 with any association order errs by at most kc * u * sum|x*y| with
+    u = 2^-23 (twice the round-to-nearest unit, so that truncating adders are
+    covered as well).
+    """
+    xa = np.abs(np.asarray(x, dtype=np.float64))
+    ya = np.abs(np.asarray(y, dtype=np.float64))
+    m, k = xa.shape
+    n = ya.shape[1]
+    if g_local is None:
+        g_local = len(group_sizes) - group_offset
+    b, _ = group_bounds(group_sizes, m, limit)
+    out = np.zeros((g_local, k, n))
+    for j in range(g_local):
+        lo, hi = b[group_offset + j], b[group_offset + j + 1]
+        if hi > lo:
+            out[j] = (hi - lo) * 2.0 ** -23 * (xa[lo:hi].T @ ya[lo:hi])
+    return out

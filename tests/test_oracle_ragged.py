@@ -411,3 +411,42 @@ def test_glu_bwd_through_down_projection_matches_finite_differences():
                 assert math.isclose(grad[i, c], fd, rel_tol=1e-6, abs_tol=1e-8), (i, c)
             else:
                 assert np.isnan(grad[i, c]) and fd == 0.0
+
+
+
+def test_dw_f32_accumulate_is_sum_of_microbatches():
+    """Accumulating two micro-batches equals one pass over their concatenation."""
+    rng = np.random.default_rng(22)
+    k, n, g = 5, 4, 3
+    x1, y1 = rng.standard_normal((20, k)), rng.standard_normal((20, n))
+    x2, y2 = rng.standard_normal((16, k)), rng.standard_normal((16, n))
+    s1, s2 = [7, 0, 13], [4, 6, 6]
+    acc = oracle.trans_ragged_dot_f32(x1, y1, s1)
+    acc = oracle.trans_ragged_dot_f32(x2, y2, s2, out_prior=acc)
+    # rows of group j from both micro-batches, stacked
+    b1, _ = oracle.group_bounds(s1, 20)
+    b2, _ = oracle.group_bounds(s2, 16)
+    xs = np.concatenate([np.concatenate([x1[b1[j]:b1[j + 1]], x2[b2[j]:b2[j + 1]]]) for j in range(g)])
+    ys = np.concatenate([np.concatenate([y1[b1[j]:b1[j + 1]], y2[b2[j]:b2[j + 1]]]) for j in range(g)])
+    sizes = [s1[j] + s2[j] for j in range(g)]
+    np.testing.assert_allclose(acc, oracle.trans_ragged_dot(xs, ys, sizes), rtol=1e-13, atol=1e-13)
+    prior = rng.standard_normal((g, k, n))
+    empty = oracle.trans_ragged_dot_f32(x1, y1, [0, 20, 0], out_prior=prior)
+    np.testing.assert_array_equal(empty[0], prior[0])       # no rows: the prior stays
+    np.testing.assert_array_equal(empty[2], prior[2])
+
+
+def test_f32_sum_bound_covers_a_sequential_f32_sum():
+    rng = np.random.default_rng(23)
+    from oracle import bf16 as obf
+    x = obf.round_to_bf16(rng.standard_normal((3000, 4)).astype(np.float32))
+    y = obf.round_to_bf16(rng.standard_normal((3000, 3)).astype(np.float32))
+    sizes = [1000, 2000]
+    ref = oracle.trans_ragged_dot(x, y, sizes)
+    bound = ragged.f32_sum_bound(x, y, sizes)
+    b, _ = oracle.group_bounds(sizes, 3000)
+    for j in range(2):
+        s = np.zeros((4, 3), np.float32)
+        for i in range(b[j], b[j + 1]):
+            s += np.outer(x[i], y[i]).astype(np.float32)
+        assert np.all(np.abs(s.astype(np.float64) - ref[j]) <= bound[j])
