@@ -269,6 +269,30 @@ def run_ops(rd, device, stream, peaks):
         del lhs, rhs, out, fused, gout, dfused
         torch.cuda.empty_cache()
 
+        # packed buffer backward through the down projection: dx (D = 4096 -> F = 1024)
+        # with the GLU backward fused, against dx followed by the standalone GLU backward
+        d_out = normal_bf16((w.m, 4096), 1.0, 35, device)
+        w_down = normal_bf16((w.g_local, 1024, 4096), 1.0 / 4096, 36, device)
+        fused2 = normal_bf16((w.m, 2048), 1.0, 37, device)
+        dfused2 = torch.empty_like(fused2)
+        dh = torch.empty((w.m, 1024), dtype=torch.bfloat16, device=device)
+        t_fused = med(lambda: rd.ragged_dot_trans_rhs_glu_bwd(d_out, w_down, fused2, gs, w.group_offset,
+                                                              lim, dfused2))
+
+        def unfused():
+            rd.ragged_dot_trans_rhs(d_out, w_down, gs, w.group_offset, lim, dh)
+            rd.glu_bwd(fused2, dh, lim, dfused2)
+
+        t_unfused = med(unfused)
+        F2 = 2.0 * rows * 1024 * 4096
+        B2 = (rows * 4096 * 2 + w.g_local * 1024 * 4096 * 2 + rows * 2048 * 2
+              + w.limit * 2048 * 2 + 4 * w.g_total)
+        res["packed_dx_glu_bwd"] = {"us": t_fused * 1e6, "unfused_us": t_unfused * 1e6,
+                                    "bound": "hbm" if B2 / BW > F2 / P else "tensor",
+                                    "frac": max(F2 / P, B2 / BW) / t_fused}
+        del d_out, w_down, fused2, dfused2, dh
+        torch.cuda.empty_cache()
+
         # valid-rows unsort backward at the packed buffer's shape [225280, 4096]
         g = normal_bf16((w.m, 4096), 1.0, 33, device)
         y = normal_bf16((w.m, 4096), 1.0, 34, device)

@@ -9,7 +9,9 @@ Functions (same names as the C ABI, without the ``rd_`` prefix):
 
 * ``ragged_dot(lhs, rhs, group_sizes, ...)``             -> out [m, n] (or [m, n/2] with GLU)
 * ``ragged_dot_trans_rhs(lhs, rhs, group_sizes, ...)``   -> out [m, k]
+* ``ragged_dot_trans_rhs_glu_bwd(d_out, rhs, fused, group_sizes, ...)`` -> [d_gate | d_up] [m, 2f]
 * ``trans_ragged_dot(x, y, group_sizes, ...)``           -> out [g_local, k, n]
+* ``trans_ragged_dot_f32(x, y, group_sizes, ..., accumulate=False)`` -> f32 out [g_local, k, n]
 * ``glu_fwd(fused, limit=None)``                         -> out [rows, f]
 * ``glu_bwd(fused, d_out, limit=None)``                  -> d_fused [rows, 2f]
 * ``unsort_bwd_rows(g, y, w, limit=None)``                -> (grad [rows, hidden], dot [rows])
@@ -21,7 +23,8 @@ import os
 from typing import Optional
 
 __all__ = [
-    "load", "lib_path", "ragged_dot", "ragged_dot_trans_rhs", "trans_ragged_dot",
+    "load", "lib_path", "ragged_dot", "ragged_dot_trans_rhs", "ragged_dot_trans_rhs_glu_bwd",
+    "trans_ragged_dot", "trans_ragged_dot_f32",
     "glu_fwd", "glu_bwd", "unsort_bwd_rows", "RdError", "EPI_NONE", "EPI_SILU_GLU",
     "STATUS_NEG_SIZE", "STATUS_OVERFLOW", "STATUS_TIMEOUT", "MAX_GROUPS",
 ]
@@ -62,11 +65,15 @@ def load():
     grouped = [vp, vp, vp, i64, i64, i64, ip, i32, i32, i32, ip]
     lib.rd_ragged_dot.argtypes = grouped + [ctypes.c_int, ip, vp]
     lib.rd_ragged_dot_trans_rhs.argtypes = grouped + [ip, vp]
+    lib.rd_ragged_dot_trans_rhs_glu_bwd.argtypes = [vp] + grouped + [ip, vp]
     lib.rd_trans_ragged_dot.argtypes = grouped + [ip, vp]
+    lib.rd_trans_ragged_dot_f32.argtypes = grouped + [i32, ip, vp]
     lib.rd_glu_fwd.argtypes = [vp, vp, i64, i64, ip, vp]
     lib.rd_glu_bwd.argtypes = [vp, vp, vp, i64, i64, ip, vp]
     lib.rd_unsort_bwd_rows.argtypes = [vp, vp, vp, vp, vp, i64, i64, ip, vp]
-    for fn in (lib.rd_ragged_dot, lib.rd_ragged_dot_trans_rhs, lib.rd_trans_ragged_dot,
+    for fn in (lib.rd_ragged_dot, lib.rd_ragged_dot_trans_rhs,
+               lib.rd_ragged_dot_trans_rhs_glu_bwd, lib.rd_trans_ragged_dot,
+               lib.rd_trans_ragged_dot_f32,
                lib.rd_glu_fwd, lib.rd_glu_bwd, lib.rd_unsort_bwd_rows):
         fn.restype = ctypes.c_int
     lib.rd_status_string.argtypes = [ctypes.c_int]
@@ -157,6 +164,33 @@ def ragged_dot_trans_rhs(lhs, rhs, group_sizes, group_offset: int = 0, limit=Non
     return out
 
 
+def ragged_dot_trans_rhs_glu_bwd(d_out, rhs, fused, group_sizes, group_offset: int = 0, limit=None,
+                                 out=None, status=None, stream=None):
+    """[d_gate | d_up] of an expert FFN from its output gradient, through the down projection.
+
+    d_out [m, n], rhs [g_local, f, n] (down weights), fused [m, 2f] (saved gate | up).
+    """
+    import torch
+
+    lib = load()
+    _bf16_2d(d_out, "d_out")
+    _bf16_2d(fused, "fused")
+    _group_args(group_sizes, limit, status)
+    if rhs.dtype != torch.bfloat16 or rhs.dim() != 3 or not rhs.is_contiguous():
+        raise ValueError("rhs must be a contiguous [g_local, f, n] bf16 CUDA tensor")
+    m, n = d_out.shape
+    g_local, f, n2 = rhs.shape
+    if n2 != n or fused.shape != (m, 2 * f):
+        raise ValueError("shapes disagree: d_out [m, n], rhs [g, f, n], fused [m, 2f]")
+    if out is None:
+        out = torch.empty((m, 2 * f), dtype=torch.bfloat16, device=d_out.device)
+    code = lib.rd_ragged_dot_trans_rhs_glu_bwd(
+        _ptr(d_out), _ptr(rhs), _ptr(fused), _ptr(out), m, f, n, _ptr(group_sizes),
+        group_sizes.numel(), group_offset, g_local, _ptr(limit), _ptr(status), _stream(stream))
+    _check(code, "rd_ragged_dot_trans_rhs_glu_bwd")
+    return out
+
+
 def trans_ragged_dot(x, y, group_sizes, group_offset: int = 0, g_local: Optional[int] = None,
                      limit=None, out=None, status=None, stream=None):
     """out[j] = x[rows_j]^T @ y[rows_j] for the local groups; x [m, k], y [m, n]."""
@@ -178,6 +212,34 @@ def trans_ragged_dot(x, y, group_sizes, group_offset: int = 0, g_local: Optional
                                    group_sizes.numel(), group_offset, g_local, _ptr(limit),
                                    _ptr(status), _stream(stream))
     _check(code, "rd_trans_ragged_dot")
+    return out
+
+
+def trans_ragged_dot_f32(x, y, group_sizes, group_offset: int = 0, g_local: Optional[int] = None,
+                         limit=None, out=None, accumulate: bool = False, status=None, stream=None):
+    """out[j] (+)= x[rows_j]^T @ y[rows_j] in f32; ``accumulate`` adds into ``out``."""
+    import torch
+
+    lib = load()
+    _bf16_2d(x, "x")
+    _bf16_2d(y, "y")
+    _group_args(group_sizes, limit, status)
+    m, k = x.shape
+    m2, n = y.shape
+    if m2 != m:
+        raise ValueError("x and y disagree on m")
+    if g_local is None:
+        g_local = group_sizes.numel() - group_offset
+    if out is None:
+        if accumulate:
+            raise ValueError("accumulate needs an existing out buffer")
+        out = torch.empty((g_local, k, n), dtype=torch.float32, device=x.device)
+    if out.dtype != torch.float32 or out.shape != (g_local, k, n) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [g_local, k, n] float32 CUDA tensor")
+    code = lib.rd_trans_ragged_dot_f32(_ptr(x), _ptr(y), _ptr(out), m, k, n, _ptr(group_sizes),
+                                       group_sizes.numel(), group_offset, g_local, _ptr(limit),
+                                       1 if accumulate else 0, _ptr(status), _stream(stream))
+    _check(code, "rd_trans_ragged_dot_f32")
     return out
 
 

@@ -205,6 +205,8 @@ extern "C" rd_status rd_ragged_dot(const void* lhs, const void* rhs, void* out, 
   a.group_offset = group_offset;
   a.g_local = g_local;
   a.glu_f = static_cast<int32_t>(n_out);
+  a.ldo = n_out;
+  a.zero_cols = static_cast<int32_t>(n_out);
   const int tile_w = glu ? kBN / 2 : kBN;
   a.n_tiles = static_cast<int32_t>((n_out + tile_w - 1) / tile_w);
   a.dw_m_tiles = 0;
@@ -218,21 +220,28 @@ extern "C" rd_status rd_ragged_dot(const void* lhs, const void* rhs, void* out, 
              : RD_ERR_CUDA;
 }
 
-extern "C" rd_status rd_ragged_dot_trans_rhs(const void* lhs, const void* rhs, void* out,
-                                             int64_t m, int64_t k, int64_t n,
-                                             const int32_t* group_sizes, int32_t g_total,
-                                             int32_t group_offset, int32_t g_local,
-                                             const int32_t* limit, int32_t* status,
-                                             rd_stream_t stream) {
+namespace {
+// rd_ragged_dot_trans_rhs, optionally followed (in the epilogue) by the SiLU-GLU
+// backward against the saved fused buffer: out = dx [m, k], or [d_gate | d_up]
+// [m, 2k] when fused != nullptr.
+rd_status trans_rhs_impl(const void* lhs, const void* rhs, const void* fused, void* out, int64_t m,
+                         int64_t k, int64_t n, const int32_t* group_sizes, int32_t g_total,
+                         int32_t group_offset, int32_t g_local, const int32_t* limit,
+                         int32_t* status, rd_stream_t stream) {
   rd_status st = check_groups(m, k, n, group_sizes, g_total, group_offset, g_local, limit, status);
   if (st != RD_OK) return st;
+  const bool glu_bwd = fused != nullptr;
+  const int64_t out_w = glu_bwd ? 2 * k : k;
   if ((m > 0 && n > 0 && lhs == nullptr) || (k > 0 && n > 0 && rhs == nullptr) ||
       (m > 0 && k > 0 && out == nullptr))
     return RD_ERR_INVALID_ARG;
-  if (!aligned16(lhs) || !aligned16(rhs) || !aligned16(out)) return RD_ERR_UNSUPPORTED;
-  if (out_aliases(out, static_cast<uint64_t>(m) * k * 2, lhs, static_cast<uint64_t>(m) * n * 2,
-                  rhs, static_cast<uint64_t>(g_local) * k * n * 2, group_sizes,
-                  static_cast<uint64_t>(g_total) * 4, limit, status))
+  if (!aligned16(lhs) || !aligned16(rhs) || !aligned16(out) || !aligned16(fused))
+    return RD_ERR_UNSUPPORTED;
+  const uint64_t ob = static_cast<uint64_t>(m) * out_w * 2;
+  if (out_aliases(out, ob, lhs, static_cast<uint64_t>(m) * n * 2, rhs,
+                  static_cast<uint64_t>(g_local) * k * n * 2, group_sizes,
+                  static_cast<uint64_t>(g_total) * 4, limit, status) ||
+      overlap(out, ob, fused, static_cast<uint64_t>(m) * 2 * k * 2))
     return RD_ERR_INVALID_ARG;
   int sms = 0;
   if ((st = current_device(&sms)) != RD_OK) return st;
@@ -257,6 +266,9 @@ extern "C" rd_status rd_ragged_dot_trans_rhs(const void* lhs, const void* rhs, v
   a.limit = limit;
   a.status = status;
   a.out = out;
+  a.aux = fused;
+  a.ldo = out_w;
+  a.zero_cols = static_cast<int32_t>(out_w);
   a.m = static_cast<int32_t>(m);
   a.kc = static_cast<int32_t>(n);
   a.n_out = static_cast<int32_t>(k);
@@ -267,24 +279,52 @@ extern "C" rd_status rd_ragged_dot_trans_rhs(const void* lhs, const void* rhs, v
   a.timeout_ns = wait_timeout_ns();
   const int grid = pair ? pair_grid(sms, ((m + 2 * kBM - 1) / (2 * kBM) + g_local) * a.n_tiles)
                         : grid_for(sms, ((m + kBM - 1) / kBM + g_local) * a.n_tiles);
-  return launch_gemm_dx(pair, ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) ==
+  return launch_gemm_dx(pair, glu_bwd, ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? RD_OK
              : RD_ERR_CUDA;
 }
+}  // namespace
 
-extern "C" rd_status rd_trans_ragged_dot(const void* x, const void* y, void* out, int64_t m,
-                                         int64_t k, int64_t n, const int32_t* group_sizes,
-                                         int32_t g_total, int32_t group_offset, int32_t g_local,
-                                         const int32_t* limit, int32_t* status,
-                                         rd_stream_t stream) {
+extern "C" rd_status rd_ragged_dot_trans_rhs(const void* lhs, const void* rhs, void* out,
+                                             int64_t m, int64_t k, int64_t n,
+                                             const int32_t* group_sizes, int32_t g_total,
+                                             int32_t group_offset, int32_t g_local,
+                                             const int32_t* limit, int32_t* status,
+                                             rd_stream_t stream) {
+  return trans_rhs_impl(lhs, rhs, nullptr, out, m, k, n, group_sizes, g_total, group_offset,
+                        g_local, limit, status, stream);
+}
+
+extern "C" rd_status rd_ragged_dot_trans_rhs_glu_bwd(const void* d_out, const void* rhs,
+                                                     const void* fused, void* d_fused, int64_t m,
+                                                     int64_t f, int64_t n,
+                                                     const int32_t* group_sizes, int32_t g_total,
+                                                     int32_t group_offset, int32_t g_local,
+                                                     const int32_t* limit, int32_t* status,
+                                                     rd_stream_t stream) {
+  if (m > 0 && f > 0 && fused == nullptr) return RD_ERR_INVALID_ARG;
+  // a null fused buffer (only possible for an empty problem) still selects the GLU form
+  static const int32_t dummy[4] = {0, 0, 0, 0};
+  return trans_rhs_impl(d_out, rhs, fused != nullptr ? fused : static_cast<const void*>(dummy),
+                        d_fused, m, f, n, group_sizes, g_total, group_offset, g_local, limit,
+                        status, stream);
+}
+
+namespace {
+// trans_ragged_dot with a bf16 (epi = kEpiNone) or f32 (kEpiF32, kEpiF32Acc) output
+rd_status trans_ragged_impl(const void* x, const void* y, void* out, int64_t m, int64_t k,
+                            int64_t n, const int32_t* group_sizes, int32_t g_total,
+                            int32_t group_offset, int32_t g_local, const int32_t* limit,
+                            int epi, int32_t* status, rd_stream_t stream) {
+  const uint64_t out_elem = epi == kEpiNone ? 2 : 4;
   rd_status st = check_groups(m, k, n, group_sizes, g_total, group_offset, g_local, limit, status);
   if (st != RD_OK) return st;
   if ((m > 0 && k > 0 && x == nullptr) || (m > 0 && n > 0 && y == nullptr) ||
       (k > 0 && n > 0 && out == nullptr))
     return RD_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y) || !aligned16(out)) return RD_ERR_UNSUPPORTED;
-  if (out_aliases(out, static_cast<uint64_t>(g_local) * k * n * 2, x,
+  if (out_aliases(out, static_cast<uint64_t>(g_local) * k * n * out_elem, x,
                   static_cast<uint64_t>(m) * k * 2, y, static_cast<uint64_t>(m) * n * 2,
                   group_sizes, static_cast<uint64_t>(g_total) * 4, limit, status))
     return RD_ERR_INVALID_ARG;
@@ -314,6 +354,8 @@ extern "C" rd_status rd_trans_ragged_dot(const void* x, const void* y, void* out
   a.kc = static_cast<int32_t>(m);
   a.n_out = static_cast<int32_t>(n);
   a.m_out = static_cast<int32_t>(k);
+  a.ldo = n;
+  a.zero_cols = static_cast<int32_t>(n);
   a.g_total = g_total;
   a.group_offset = group_offset;
   a.g_local = g_local;
@@ -323,10 +365,31 @@ extern "C" rd_status rd_trans_ragged_dot(const void* x, const void* y, void* out
   const int64_t tiles = static_cast<int64_t>(g_local) * a.dw_m_tiles * a.n_tiles;
   if (tiles > kMaxDim) return RD_ERR_UNSUPPORTED;
   const int grid = pair ? pair_grid(sms, tiles) : grid_for(sms, tiles);
-  return launch_gemm_dw(pair, ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) ==
+  return launch_gemm_dw(pair, epi, ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? RD_OK
              : RD_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" rd_status rd_trans_ragged_dot(const void* x, const void* y, void* out, int64_t m,
+                                         int64_t k, int64_t n, const int32_t* group_sizes,
+                                         int32_t g_total, int32_t group_offset, int32_t g_local,
+                                         const int32_t* limit, int32_t* status,
+                                         rd_stream_t stream) {
+  return trans_ragged_impl(x, y, out, m, k, n, group_sizes, g_total, group_offset, g_local, limit,
+                           kEpiNone, status, stream);
+}
+
+extern "C" rd_status rd_trans_ragged_dot_f32(const void* x, const void* y, float* out, int64_t m,
+                                             int64_t k, int64_t n, const int32_t* group_sizes,
+                                             int32_t g_total, int32_t group_offset,
+                                             int32_t g_local, const int32_t* limit,
+                                             int32_t accumulate, int32_t* status,
+                                             rd_stream_t stream) {
+  if (accumulate != 0 && accumulate != 1) return RD_ERR_INVALID_ARG;
+  return trans_ragged_impl(x, y, out, m, k, n, group_sizes, g_total, group_offset, g_local, limit,
+                           accumulate ? kEpiF32Acc : kEpiF32, status, stream);
 }
 
 namespace {

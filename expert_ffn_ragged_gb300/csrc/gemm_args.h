@@ -14,12 +14,21 @@ enum GemmOp : int {
   kOpDw = 2    // out[j] = x[rows_j]^T @ y[rows_j]     (A MN-major, B MN-major)
 };
 
+// What the epilogue does with the f32 accumulator.
+enum GemmEpi : int {
+  kEpiNone = 0,   // round to bf16 and store
+  kEpiGlu = 1,    // forward: silu(gate) * up from the gate / up halves of the tile
+  kEpiGluBwd = 2,  // dx of the down projection: [d_gate | d_up] from dh and the saved [gate | up]
+  kEpiF32 = 3,     // dw: store the f32 accumulator as is
+  kEpiF32Acc = 4   // dw: add the f32 accumulator to the f32 output already in memory
+};
+
 // UMMA tile: 128 x 256 f32 accumulator per CTA, 64-deep K blocks (one
 // 128-byte swizzle atom of bf16).
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warps 6-7 zero fill
+constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warp 6 zero fill
 constexpr int kTmemCols = 2 * kBN;  // two accumulators (double buffer)
 constexpr int kMaxGroups = 1024;
 
@@ -28,6 +37,9 @@ struct GemmArgs {
   const int32_t* limit;        // device scalar or null
   int32_t* status;             // device or null
   void* out;                   // bf16 output
+  const void* aux;             // kEpiGluBwd: the saved fused [gate | up] buffer [m, 2 * n_out]
+  int64_t ldo;                 // row stride of out (elements)
+  int32_t zero_cols;           // columns of a zero row (n_out, or 2 * n_out for kEpiGluBwd)
   int32_t m;                   // token rows
   int32_t kc;                  // contraction length (fwd: k, dx: n); dw: unused (rows of each group)
   int32_t n_out;               // output width (columns stored)
@@ -46,10 +58,12 @@ struct GemmArgs {
 cudaError_t launch_gemm_fwd(bool glu, bool pair, const CUtensorMap& tmap_a,
                             const CUtensorMap& tmap_b, const GemmArgs& args, int grid,
                             cudaStream_t stream);
-cudaError_t launch_gemm_dx(bool pair, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                           const GemmArgs& args, int grid, cudaStream_t stream);
-cudaError_t launch_gemm_dw(bool pair, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
-                           const GemmArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_dx(bool pair, bool glu_bwd, const CUtensorMap& tmap_a,
+                           const CUtensorMap& tmap_b, const GemmArgs& args, int grid,
+                           cudaStream_t stream);
+cudaError_t launch_gemm_dw(bool pair, int epi, const CUtensorMap& tmap_a,
+                           const CUtensorMap& tmap_b, const GemmArgs& args, int grid,
+                           cudaStream_t stream);
 
 cudaError_t launch_glu_fwd(const void* fused, void* out, int32_t rows, int32_t f,
                            const int32_t* limit, int grid, cudaStream_t stream);

@@ -24,7 +24,8 @@
 //     TMEM accumulators; warps 2-5 drain the other accumulator with
 //     tcgen05.ld, round to bf16 (or apply the GLU) and store full 64-byte row
 //     segments through a small shared-memory transpose, with row masks;
-//     warps 6-7 write the zero rows of the forward/dx outputs;
+//     warp 6 has the bulk-copy engine write the zero rows of the forward/dx
+//     outputs from a zero block in shared memory;
 //   * PAIR=false: one CTA per SM computes a 128x256 tile (UMMA 128x256x16,
 //     4-stage ring of 48 KB).  PAIR=true: a cluster of two CTAs computes a
 //     256x256 tile with the CTA-pair UMMA (cta_group::2, 256x256x16): each
@@ -86,7 +87,9 @@ struct alignas(16) GemmShared {
   int32_t zero_hi;  // forward/dx: rows [zero_hi, L) are zero
   int32_t bound[kMaxGroups + 1];       // group boundaries, clamped to L
   int32_t tile_start[kMaxGroups + 1];  // first tile of each local group
-  uint4 epi[4][32 * 4];                // epilogue staging: 32 rows x 64 bytes per warp
+  uint4 epi[4][32 * 8];                // epilogue staging per warp: 32 rows x 128 bytes
+                                       // (two 64-byte halves for bf16 chunks)
+  uint4 zeros[256];                    // 4 KB zero block, the source of the zero-fill copies
 };
 
 template <bool PAIR>
@@ -255,10 +258,14 @@ __device__ __forceinline__ void dw_zero_rows(uint8_t* a_st, uint8_t* b_st, int z
   ptx::fence_proxy_async_smem();
 }
 
-template <int OP, bool GLU, bool PAIR>
+template <int OP, int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                         const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
+  constexpr bool GLU = (EPI == kEpiGlu);
+  static_assert(EPI != kEpiGluBwd || OP == kOpDx, "the GLU backward epilogue follows dx");
+  static_assert((EPI != kEpiF32 && EPI != kEpiF32Acc) || OP == kOpDw, "f32 output is for dw");
+  constexpr bool F32OUT = (EPI == kEpiF32 || EPI == kEpiF32Acc);
   using Cfg = TileCfg<PAIR>;
   constexpr int S = Cfg::kStagesN;
   constexpr int TM = Cfg::kTileM;
@@ -564,30 +571,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lo = OP == kOpDw ? 0 : tl.rs + tl.m_idx * TM;
       const int hi = OP == kOpDw ? args.m_out : tl.re;
       __nv_bfloat16* base =
-          OP == kOpDw ? out + static_cast<size_t>(tl.j) * args.m_out * args.n_out : out;
+          OP == kOpDw ? out + static_cast<size_t>(tl.j) * args.m_out * args.ldo : out;
       const int col0 = tl.n_idx * tile_w;
       // write the 16 packed words of this lane's row into the staging buffer, then
       // store the chunk's 32 rows x 32 columns to global memory
-      auto emit = [&](const uint32_t (&p)[16], int col) {
+      // (col_off shifts the destination, e.g. to the d_up half of a fused row)
+      auto emit = [&](const uint32_t (&p)[16], int col, int col_off, uint4* buf) {
 #pragma unroll
         for (int v = 0; v < 4; ++v)
-          stg[lane * 4 + (v ^ ((lane >> 1) & 3))] =
+          buf[lane * 4 + (v ^ ((lane >> 1) & 3))] =
               make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
         __syncwarp();
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
           const int rl = it * 8 + sr;
-          const uint4 val = stg[rl * 4 + (piece ^ ((rl >> 1) & 3))];
+          const uint4 val = buf[rl * 4 + (piece ^ ((rl >> 1) & 3))];
           const int row = wrow0 + rl;
           const int c = col + piece * 8;
           if (row >= lo && row < hi && c + 8 <= args.n_out)
-            *reinterpret_cast<uint4*>(base + static_cast<size_t>(row) * args.n_out + c) = val;
+            *reinterpret_cast<uint4*>(base + static_cast<size_t>(row) * args.ldo + col_off + c) = val;
+        }
+        __syncwarp();
+      };
+      // f32 output of dw: 32 rows x 32 columns (128 bytes a row) per chunk, stored
+      // 4 rows x 128 contiguous bytes per instruction; the accumulating form adds
+      // the chunk to what the output already holds
+      auto emit_f32 = [&](const uint32_t (&v)[32], int col) {
+        uint4* buf = sh.epi[q];
+#pragma unroll
+        for (int pc = 0; pc < 8; ++pc)
+          buf[lane * 8 + (pc ^ (lane & 7))] =
+              make_uint4(v[4 * pc], v[4 * pc + 1], v[4 * pc + 2], v[4 * pc + 3]);
+        __syncwarp();
+        float* outf = reinterpret_cast<float*>(args.out) +
+                      static_cast<size_t>(tl.j) * args.m_out * args.ldo;
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int rl = it * 4 + (lane >> 3);
+          const int pc = lane & 7;
+          uint4 val = buf[rl * 8 + (pc ^ (rl & 7))];
+          const int row = wrow0 + rl;
+          const int c = col + pc * 4;
+          if (row < hi && c + 4 <= args.n_out) {
+            uint4* dst = reinterpret_cast<uint4*>(outf + static_cast<size_t>(row) * args.ldo + c);
+            if (EPI == kEpiF32Acc) {
+              const uint4 o = *dst;
+              val = make_uint4(__float_as_uint(__fadd_rn(__uint_as_float(o.x), __uint_as_float(val.x))),
+                               __float_as_uint(__fadd_rn(__uint_as_float(o.y), __uint_as_float(val.y))),
+                               __float_as_uint(__fadd_rn(__uint_as_float(o.z), __uint_as_float(val.z))),
+                               __float_as_uint(__fadd_rn(__uint_as_float(o.w), __uint_as_float(val.w))));
+            }
+            *dst = val;
+          }
         }
         __syncwarp();
       };
       if (tl.nkb == 0) {
+        if (F32OUT) {
+          if (EPI == kEpiF32) {  // an empty group's block is zero (accumulating: unchanged)
+            const uint32_t z[32] = {};
+            for (int c = 0; c < tile_w / 32; ++c) emit_f32(z, col0 + c * 32);
+          }
+          continue;
+        }
         const uint32_t z[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
-        for (int c = 0; c < tile_w / 32; ++c) emit(z, col0 + c * 32);
+        for (int c = 0; c < tile_w / 32; ++c) {
+          emit(z, col0 + c * 32, 0, stg);
+          if (EPI == kEpiGluBwd) emit(z, col0 + c * 32, args.n_out, stg);
+        }
         continue;
       }
       bool ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.tfull[acc]), acc_phase, abort_flag,
@@ -608,7 +659,57 @@ __global__ void __launch_bounds__(kThreads, 1)
             p[i] = pack_bf16x2(glu_fwd_f32(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
                                glu_fwd_f32(__uint_as_float(g[2 * i + 1]),
                                            __uint_as_float(u[2 * i + 1])));
-          emit(p, col0 + c * 32);
+          emit(p, col0 + c * 32, 0, stg);
+        }
+      } else if (EPI == kEpiGluBwd) {
+        // dh (f32, this tile's accumulator) meets the saved gate / up of the same rows:
+        // both are staged through shared memory with coalesced loads, the backward of
+        // the GLU runs per element in f32, and [d_gate | d_up] leave through emit().
+        const __nv_bfloat16* fused = reinterpret_cast<const __nv_bfloat16*>(args.aux);
+        uint4* stg2 = sh.epi[q] + 32 * 4;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          const int col = col0 + c * 32;
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int rl = it * 8 + sr;
+            const int row = wrow0 + rl;
+            const int cc = col + piece * 8;
+            if (row >= lo && row < hi && cc + 8 <= args.n_out) {
+              const __nv_bfloat16* src = fused + static_cast<size_t>(row) * (2 * args.n_out) + cc;
+              const int slot = rl * 4 + (piece ^ ((rl >> 1) & 3));
+              stg[slot] = __ldg(reinterpret_cast<const uint4*>(src));
+              stg2[slot] = __ldg(reinterpret_cast<const uint4*>(src + args.n_out));
+            }
+          }
+          uint32_t v[32], pg[16], pu[16];
+          ptx::tmem_load_32cols(tbase + c * 32, v);
+          __syncwarp();
+#pragma unroll
+          for (int w4 = 0; w4 < 4; ++w4) {
+            const int slot = lane * 4 + (w4 ^ ((lane >> 1) & 3));
+            const uint4 G = stg[slot], U = stg2[slot];
+            const uint32_t gw[4] = {G.x, G.y, G.z, G.w}, uw[4] = {U.x, U.y, U.z, U.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              float dg0, du0, dg1, du1;
+              glu_bwd_f32(bf16_lo(gw[i]), bf16_lo(uw[i]), __uint_as_float(v[w4 * 8 + 2 * i]), dg0, du0);
+              glu_bwd_f32(bf16_hi(gw[i]), bf16_hi(uw[i]), __uint_as_float(v[w4 * 8 + 2 * i + 1]), dg1,
+                          du1);
+              pg[w4 * 4 + i] = bf16x2_neg_zero_to_pos(pack_bf16x2(dg0, dg1));
+              pu[w4 * 4 + i] = bf16x2_neg_zero_to_pos(pack_bf16x2(du0, du1));
+            }
+          }
+          __syncwarp();
+          emit(pg, col, 0, stg);
+          emit(pu, col, args.n_out, stg2);
+        }
+      } else if (F32OUT) {
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          ptx::tmem_load_32cols(tbase + c * 32, v);
+          emit_f32(v, col0 + c * 32);
         }
       } else {
 #pragma unroll 1
@@ -618,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             p[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          emit(p, col0 + c * 32);
+          emit(p, col0 + c * 32, 0, stg);
         }
       }
       ptx::tc_fence_before();
@@ -632,20 +733,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
-  } else if (OP != kOpDw) {
+  } else if (OP != kOpDw && warp == 6) {
     // ------------------------------------------------------------ zero fill
-    // rows [0, zero_lo) and [zero_hi, L): this CTA's contiguous share of them
-    const long long zlo = sh.zero_lo;
-    const long long zhi_n = sh.L - sh.zero_hi;
-    const long long Z = zlo + zhi_n;
-    const long long r0 = Z * blockIdx.x / gridDim.x;
-    const long long r1 = Z * (blockIdx.x + 1) / gridDim.x;
-    const int vpr = args.n_out / 8;
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
-    for (long long rc = r0 + (warp - 6); rc < r1; rc += 2) {
-      const long long row = rc < zlo ? rc : sh.zero_hi + (rc - zlo);
-      uint4* p = reinterpret_cast<uint4*>(out + row * args.n_out);
-      for (int v = lane; v < vpr; v += 32) p[v] = make_uint4(0, 0, 0, 0);
+    // Rows [0, zero_lo) and [zero_hi, L) are two contiguous byte ranges of the
+    // output (its rows are contiguous).  Each CTA takes a contiguous 16-byte
+    // aligned share of their concatenation and has the bulk-copy engine write it
+    // from a 4 KB zero block in shared memory.
+    for (int i = lane; i < 256; i += 32) sh.zeros[i] = make_uint4(0, 0, 0, 0);
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      const uint64_t row_bytes = static_cast<uint64_t>(args.ldo) * 2;
+      const uint64_t lo_bytes = static_cast<uint64_t>(sh.zero_lo) * row_bytes;
+      const uint64_t z_bytes = lo_bytes + static_cast<uint64_t>(sh.L - sh.zero_hi) * row_bytes;
+      const uint64_t units16 = z_bytes / 16;
+      const uint64_t b0 = units16 * blockIdx.x / gridDim.x * 16;
+      const uint64_t b1 = units16 * (blockIdx.x + 1) / gridDim.x * 16;
+      char* base = reinterpret_cast<char*>(args.out);
+      const uint32_t src = ptx::smem_addr(sh.zeros);
+      uint64_t b = b0;
+      while (b < b1) {
+        const bool low = b < lo_bytes;
+        const uint64_t seg_end = low ? lo_bytes : z_bytes;
+        const uint64_t addr = low ? b : static_cast<uint64_t>(sh.zero_hi) * row_bytes + (b - lo_bytes);
+        uint64_t len = (b1 < seg_end ? b1 : seg_end) - b;
+        if (len > 4096) len = 4096;
+        ptx::bulk_copy_s2g(base + addr, src, static_cast<uint32_t>(len));
+        b += len;
+      }
+      ptx::bulk_commit();
+      ptx::bulk_wait_read_all();
     }
   }
 
@@ -661,20 +778,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicOr(args.status, RD_STATUS_TIMEOUT);
 }
 
-template <int OP, bool GLU, bool PAIR>
+template <int OP, int EPI, bool PAIR>
 cudaError_t launch_gemm_impl(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                              const GemmArgs& args, int grid, cudaStream_t stream) {
   constexpr size_t smem = gemm_smem_bytes_t<PAIR>();
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<OP, GLU, PAIR>,
+    const cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<OP, EPI, PAIR>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   if (!PAIR) {
-    grouped_gemm_kernel<OP, GLU, PAIR><<<grid, kThreads, smem, stream>>>(tmap_a, tmap_b, args);
+    grouped_gemm_kernel<OP, EPI, PAIR><<<grid, kThreads, smem, stream>>>(tmap_a, tmap_b, args);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -697,13 +814,13 @@ cudaError_t launch_gemm_impl(const CUtensorMap& tmap_a, const CUtensorMap& tmap_
   if (max_clusters[dev] == 0) {
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     int n = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<OP, GLU, PAIR>, &cfg);
+    const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<OP, EPI, PAIR>, &cfg);
     if (e != cudaSuccess) return e;
     max_clusters[dev] = n > 0 ? n : 1;
   }
   if (grid > 2 * max_clusters[dev]) grid = 2 * max_clusters[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<OP, GLU, PAIR>, tmap_a, tmap_b, args);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<OP, EPI, PAIR>, tmap_a, tmap_b, args);
 }
 
 }  // namespace rd

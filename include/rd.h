@@ -116,6 +116,35 @@ rd_status rd_ragged_dot_trans_rhs(const void* lhs, const void* rhs, void* out, i
                                   const int32_t* limit, int32_t* status, rd_stream_t stream);
 
 /*
+ * rd_ragged_dot_trans_rhs_glu_bwd -- dx of an expert FFN's down projection with
+ * the SiLU-GLU backward fused into its epilogue.
+ *   dh[i, c]         = sum_n d_out[i, n] * rhs[j, c, n]      (f32, never stored)
+ *   g = fused[i, c], u = fused[i, f + c], e = exp(-g), den = 1 + e,
+ *   sig = 1 / den, silu = g / den                           (f32)
+ *   d_fused[i, c]     = bf16((dh * u) * (sig * (1 + g * (1 - sig))))   (d_gate)
+ *   d_fused[i, f + c] = bf16(dh * silu)                                (d_up)
+ *   with -0 stored as +0, for every row i of local group j; rows in [0, L)
+ *   outside the local groups are +0 in both halves; rows >= L untouched.
+ * Defined by SkyRL PR #867 (trans_rhs form of the backward) and MaxText PR
+ * #5760 (commit message: the GLU backward writes [d_gate | d_up] in one pass,
+ * recomputing the forward from the saved fused buffer).  Unlike running
+ * rd_ragged_dot_trans_rhs then rd_glu_bwd, dh is used unrounded and never
+ * goes to memory.
+ *
+ *   d_out [m, n] bf16, rhs [g_local, f, n] bf16 (the down weights, forward
+ *   h [m, f] @ rhs[j] [f, n]), fused [m, 2f] bf16, d_fused [m, 2f] bf16.
+ *   Other arguments as rd_ragged_dot.
+ * Requires f % 8 == 0, n % 8 == 0, 16-byte aligned pointers; d_fused must
+ * not overlap any input.
+ */
+rd_status rd_ragged_dot_trans_rhs_glu_bwd(const void* d_out, const void* rhs, const void* fused,
+                                          void* d_fused, int64_t m, int64_t f, int64_t n,
+                                          const int32_t* group_sizes, int32_t g_total,
+                                          int32_t group_offset, int32_t g_local,
+                                          const int32_t* limit, int32_t* status,
+                                          rd_stream_t stream);
+
+/*
  * rd_trans_ragged_dot -- per-group weight gradient.
  *   out[j, :, :] = x[rows_j, :]^T @ y[rows_j, :] for each local group j;
  *   a group without rows (or whose rows all lie at or past L) gives zeros.
@@ -131,6 +160,24 @@ rd_status rd_trans_ragged_dot(const void* x, const void* y, void* out, int64_t m
                               int64_t n, const int32_t* group_sizes, int32_t g_total,
                               int32_t group_offset, int32_t g_local, const int32_t* limit,
                               int32_t* status, rd_stream_t stream);
+
+/*
+ * rd_trans_ragged_dot_f32 -- per-group weight gradient kept in f32, optionally
+ * accumulated into the output (gradient accumulation across micro-batches).
+ *   accumulate = 0: out[j] = x[rows_j]^T @ y[rows_j]   (a group without rows: zeros)
+ *   accumulate = 1: out[j] += x[rows_j]^T @ y[rows_j]  (a group without rows: unchanged)
+ * The sum is the tensor cores' f32 accumulation; the add of the accumulating
+ * form rounds once, to nearest.  SkyRL PR #867 (_gpu_trans_ragged_dot_fwd
+ * separates acc_dtype = f32 from the compute dtype).
+ *
+ *   x [m, k] bf16, y [m, n] bf16, out [g_local, k, n] f32.  Other arguments as
+ *   rd_trans_ragged_dot.  Calls that accumulate into the same buffer must be
+ *   ordered on one stream.
+ */
+rd_status rd_trans_ragged_dot_f32(const void* x, const void* y, float* out, int64_t m, int64_t k,
+                                  int64_t n, const int32_t* group_sizes, int32_t g_total,
+                                  int32_t group_offset, int32_t g_local, const int32_t* limit,
+                                  int32_t accumulate, int32_t* status, rd_stream_t stream);
 
 /*
  * rd_glu_fwd -- SiLU-GLU forward over the valid rows of a fused buffer.

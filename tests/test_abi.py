@@ -24,18 +24,19 @@ def lib():
 def _declared():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(rd_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(rd_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_abi():
     assert _declared() == sorted([
         "rd_glu_bwd", "rd_glu_fwd", "rd_ragged_dot", "rd_ragged_dot_trans_rhs",
-        "rd_status_string", "rd_trans_ragged_dot", "rd_unsort_bwd_rows"])
+        "rd_ragged_dot_trans_rhs_glu_bwd", "rd_status_string", "rd_trans_ragged_dot",
+        "rd_trans_ragged_dot_f32", "rd_unsort_bwd_rows"])
 
 
 def test_every_declared_symbol_is_exported(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True)
-    exported = set(re.findall(r"\bT (rd_[a-z_]+)\b", out.stdout))
+    exported = set(re.findall(r"\bT (rd_[a-z0-9_]+)\b", out.stdout))
     for name in _declared():
         assert name in exported, name
         assert getattr(lib, name) is not None
@@ -93,6 +94,17 @@ def test_other_entry_points_check_arguments(lib):
         assert f(P, P * 0x100, P * 0x10000, 16, 64, 64, None, 4, 0, 4, None, None, None) == RD_ERR_INVALID_ARG
         assert f(P, P * 0x100, P * 0x10000, 16, 60, 64, P * 0x1000000, 4, 0, 4, None, None, None) == RD_ERR_UNSUPPORTED
         assert f(P, P * 0x100, P, 16, 64, 64, P * 0x1000000, 4, 0, 4, None, None, None) == RD_ERR_INVALID_ARG
+    f = lib.rd_ragged_dot_trans_rhs_glu_bwd
+    f.restype = ctypes.c_int
+    f.argtypes = [v, v, v, v, i64, i64, i64, v, i32, i32, i32, v, v, v]
+    assert f(P, P * 0x100, None, P * 0x10000, 16, 64, 64, P * 0x1000000, 4, 0, 4, None, None, None) == RD_ERR_INVALID_ARG
+    assert f(P, P * 0x100, P * 0x200, P * 0x200, 16, 64, 64, P * 0x1000000, 4, 0, 4, None, None, None) == RD_ERR_INVALID_ARG
+    assert f(P, P * 0x100, P * 0x200, P * 0x10000, 16, 60, 64, P * 0x1000000, 4, 0, 4, None, None, None) == RD_ERR_UNSUPPORTED
+    f = lib.rd_trans_ragged_dot_f32
+    f.restype = ctypes.c_int
+    f.argtypes = [v, v, v, i64, i64, i64, v, i32, i32, i32, v, i32, v, v]
+    assert f(P, P * 0x100, P * 0x10000, 16, 64, 64, P * 0x1000000, 4, 0, 4, None, 2, None, None) == RD_ERR_INVALID_ARG
+    assert f(P, P * 0x100, P * 0x10000, 16, 60, 64, P * 0x1000000, 4, 0, 4, None, 1, None, None) == RD_ERR_UNSUPPORTED
     lib.rd_glu_fwd.restype = ctypes.c_int
     lib.rd_glu_fwd.argtypes = [v, v, i64, i64, v, v]
     assert lib.rd_glu_fwd(P, P * 0x100, 16, 12, None, None) == RD_ERR_UNSUPPORTED

@@ -233,6 +233,45 @@ def test_dx(rd_lib, m, k, n, off, gl, limit):
     run_dx(rd_lib, m, k, n, EDGE_SIZES, off=off, gl=gl, limit=limit, seed=k + n + off)
 
 
+# ------------------------------------------------------------------ dx + fused GLU backward
+def run_dx_glu_bwd(rd, m, f, n, sizes, off=0, gl=None, limit=None, seed=0):
+    rng = np.random.default_rng(seed)
+    gl = len(sizes) - off if gl is None else gl
+    d_out = _normal(rng, (m, n))
+    w = _normal(rng, (gl, f, n), 1.0 / n)
+    fused = _normal(rng, (m, 2 * f), 4.0)
+    b, L = oracle.group_bounds(sizes, m, limit)
+    d_dev, f_dev = d_out.clone(), fused.clone()
+    d_dev[L:] = float("nan")
+    f_dev[L:] = float("nan")
+    buf = _sentinel_buffer(m, 2 * f)
+    rd.ragged_dot_trans_rhs_glu_bwd(d_dev.to(DEV), w.to(DEV), f_dev.to(DEV), _i32(sizes),
+                                    group_offset=off,
+                                    limit=None if limit is None else _i32([limit]), out=buf[:m])
+    torch.cuda.synchronize()
+    bits = obf.torch_bf16_bits(buf)
+    got = _f64(buf[:m])
+    d64, w64, f64 = _f64(d_out), _f64(w), _f64(fused)
+    local = np.zeros(m, bool)
+    local[b[off]:b[off + gl]] = True
+    _check_rows(bits, m, L, local)
+    assert not np.any(bits[:m][local] == 0x8000), "a -0 survived the -0 -> +0 fix"
+    ref = oracle.ragged_dot_trans_rhs_glu_bwd(d64, w64, f64, sizes, off, limit)
+    # dh carries the GEMM error E; it enters d_gate with |u * dsilu| and d_up with |silu|
+    E = 1e-3 * math.sqrt(n) * (np.abs(d64[:L]).max() if L else 0.0) * np.abs(w64).max()
+    from oracle import glu as oglu
+    dg1, du1 = oglu.glu_bwd_f64(f64[:, :f], f64[:, f:], 1.0)
+    tol = obf.ulp(ref) + np.concatenate([np.abs(dg1), np.abs(du1)], axis=1) * E
+    assert_close(got[local], ref[local], tol[local], "dx + GLU backward")
+
+
+@pytest.mark.parametrize("m,f,n,off,gl,limit", [(700, 136, 264, 0, 8, None), (700, 256, 128, 2, 4, 500),
+                                                (643, 64, 520, 0, 8, 600), (1800, 512, 128, 1, 5, 1500)])
+def test_dx_glu_bwd(rd_lib, m, f, n, off, gl, limit):
+    sizes = EDGE_SIZES if m < 1800 else PAIR_EDGE_SIZES
+    run_dx_glu_bwd(rd_lib, m, f, n, sizes, off=off, gl=gl, limit=limit, seed=f + n + off)
+
+
 # ------------------------------------------------------------------ dw
 DW_SIZES = [0, 1, 63, 64, 65, 200, 0, 130]   # sum 523
 
@@ -241,6 +280,71 @@ DW_SIZES = [0, 1, 63, 64, 65, 200, 0, 130]   # sum 523
                                                 (523, 264, 72, 0, 8, 523), (600, 64, 520, 3, 4, 130)])
 def test_dw(rd_lib, m, k, n, off, gl, limit):
     run_dw(rd_lib, m, k, n, DW_SIZES, off=off, gl=gl, limit=limit, seed=k + n + off)
+
+
+def run_dw_f32(rd, m, k, n, sizes, off=0, gl=None, limit=None, seed=0, accumulate=False):
+    from oracle import ragged
+    rng = np.random.default_rng(seed)
+    gl = len(sizes) - off if gl is None else gl
+    x = _normal(rng, (m, k))
+    y = _normal(rng, (m, n))
+    b, L = oracle.group_bounds(sizes, m, limit)
+    x_dev, y_dev = x.clone(), y.clone()
+    x_dev[L:] = float("nan")
+    y_dev[L:] = float("nan")
+    if b[off] > 0:
+        x_dev[: b[off]] = float("nan")
+        y_dev[: b[off]] = float("nan")
+    prior = torch.from_numpy(rng.standard_normal((gl, k, n)).astype(np.float32))
+    out = prior.clone().to(DEV) if accumulate else torch.full((gl, k, n), float("nan"), device=DEV)
+    rd.trans_ragged_dot_f32(x_dev.to(DEV), y_dev.to(DEV), _i32(sizes), group_offset=off, g_local=gl,
+                            limit=None if limit is None else _i32([limit]), out=out,
+                            accumulate=accumulate)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    x64, y64 = _f64(x), _f64(y)
+    p64 = prior.numpy().astype(np.float64)
+    ref = oracle.trans_ragged_dot_f32(x64, y64, sizes, off, gl, limit,
+                                      out_prior=p64 if accumulate else None)
+    bound = ragged.f32_sum_bound(x64, y64, sizes, off, gl, limit)
+    # the accumulating form also rounds its final f32 add
+    tol = bound + (np.abs(np.spacing(ref.astype(np.float32))).astype(np.float64) if accumulate else 0.0)
+    for j in range(gl):
+        if b[off + j + 1] == b[off + j]:
+            want = p64[j] if accumulate else np.zeros_like(p64[j])
+            np.testing.assert_array_equal(got[j], want)
+            continue
+        assert_close(got[j], ref[j], tol[j], f"dw f32 group {j}")
+
+
+@pytest.mark.parametrize("accumulate", [False, True])
+@pytest.mark.parametrize("m,k,n,off,gl,limit", [(600, 136, 264, 0, 8, None), (600, 128, 256, 2, 5, 400),
+                                                (523, 264, 72, 0, 8, 523)])
+def test_dw_f32(rd_lib, m, k, n, off, gl, limit, accumulate):
+    run_dw_f32(rd_lib, m, k, n, DW_SIZES, off=off, gl=gl, limit=limit, seed=k + n + off,
+               accumulate=accumulate)
+
+
+def test_dw_f32_accumulates_microbatches(rd_lib):
+    """Two accumulating calls equal one call over both micro-batches' rows."""
+    rng = np.random.default_rng(31)
+    k, n = 128, 256
+    s1, s2 = [300, 0, 212], [100, 250, 162]
+    x1, y1 = _normal(rng, (512, k)).to(DEV), _normal(rng, (512, n)).to(DEV)
+    x2, y2 = _normal(rng, (512, k)).to(DEV), _normal(rng, (512, n)).to(DEV)
+    acc = torch.zeros((3, k, n), dtype=torch.float32, device=DEV)
+    rd_lib.trans_ragged_dot_f32(x1, y1, _i32(s1), out=acc, accumulate=True)
+    rd_lib.trans_ragged_dot_f32(x2, y2, _i32(s2), out=acc, accumulate=True)
+    torch.cuda.synchronize()
+    b1, _ = oracle.group_bounds(s1, 512)
+    b2, _ = oracle.group_bounds(s2, 512)
+    xs = torch.cat([torch.cat([x1[b1[j]:b1[j + 1]], x2[b2[j]:b2[j + 1]]]) for j in range(3)])
+    ys = torch.cat([torch.cat([y1[b1[j]:b1[j + 1]], y2[b2[j]:b2[j + 1]]]) for j in range(3)])
+    sizes = [s1[j] + s2[j] for j in range(3)]
+    from oracle import ragged
+    ref = oracle.trans_ragged_dot(_f64(xs), _f64(ys), sizes)
+    bound = ragged.f32_sum_bound(_f64(xs), _f64(ys), sizes) * 2 + np.abs(np.spacing(ref.astype(np.float32)))
+    assert_close(acc.cpu().numpy(), ref, bound, "two accumulated micro-batches")
 
 
 def test_dw_all_groups_empty(rd_lib):
