@@ -18,8 +18,10 @@ Also reported on the same line:
                 workload on this host's cores;
   ops           the other rows of the hot path at their own workloads
                 (packed GLU forward, dx, dw, decode pair in one CUDA graph,
-                standalone GLU forward/backward, unsort backward), each as
-                time per call and fraction of its roofline.
+                standalone GLU forward/backward, unsort backward, the fused
+                GLU backward through the down projection, and the expert FFN
+                forward graph from 256 to 16384 tokens), each as time per call
+                and fraction of its roofline.
 
 --impl reference times the oracle itself as the reference arm.
 Under torchrun (--gpus N) every rank runs an independent replica (no
@@ -359,7 +361,59 @@ def run_ops(rd, device, stream, peaks):
                         "pair_frac": (B_up + B_dn) / BW / t_pair}
             del lhs, up, down, h, o, g
             torch.cuda.empty_cache()
+        # the expert FFN forward (up with GLU, then down) as one CUDA graph, from decode
+        # to prefill batch sizes: where the weight stream stops bounding the time
+        res["ffn_sweep"] = ffn_sweep(rd, device, stream, peaks)
     return res
+
+
+def ffn_sweep(rd, device, stream, peaks, tokens=(256, 1024, 4096, 16384)):
+    """Up (GLU) + down projections of 128 experts (4096 -> 1536 -> 4096), top-8 routing."""
+    import numpy as np
+    import torch
+
+    from workloads import normal_bf16, topk_counts
+
+    P = peaks["bf16_tflops"] * 1e12
+    BW = peaks["hbm_gbs"] * 1e9
+    g, k, n = 128, 4096, 1536
+    up = normal_bf16((g, k, n), 1.0 / k, 61, device)
+    down = normal_bf16((g, n // 2, k), 1.0 / (n // 2), 62, device)
+    rows_out = []
+    for t in tokens:
+        rng = np.random.default_rng(t)
+        logits = rng.standard_normal((t, g)) + rng.standard_normal(g)
+        sizes = topk_counts(logits, 8)
+        m = int(sizes.sum())
+        lhs = normal_bf16((m, k), 1.0, 63, device)
+        gs = torch.tensor(sizes, dtype=torch.int32, device=device)
+        h = torch.empty((m, n // 2), dtype=torch.bfloat16, device=device)
+        o = torch.empty((m, k), dtype=torch.bfloat16, device=device)
+
+        def pair():
+            rd.ragged_dot(lhs, up, gs, epilogue=rd.EPI_SILU_GLU, out=h)
+            rd.ragged_dot(h, down, gs, out=o)
+
+        with torch.cuda.stream(stream):
+            pair()
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                pair()
+            per, _ = time_launches(graph.replay, 20, 3, stream)
+        tsec = statistics.median(per) * 1e-3
+        live = int((sizes > 0).sum())
+        flops = 2.0 * m * k * n + 2.0 * m * (n // 2) * k
+        byts = (m * k * 2 + live * k * n * 2 + m * (n // 2) * 2) + \
+               (m * (n // 2) * 2 + live * (n // 2) * k * 2 + m * k * 2)
+        rows_out.append({"tokens": t, "rows": m, "live_groups": live, "us": tsec * 1e6,
+                         "tflops": flops / tsec / 1e12, "gbs": byts / tsec / 1e9,
+                         "bound": "tensor" if flops / P > byts / BW else "hbm",
+                         "frac": max(flops / P, byts / BW) / tsec})
+        del lhs, gs, h, o, graph
+    del up, down
+    torch.cuda.empty_cache()
+    return rows_out
 
 
 # ----------------------------------------------------------------- arms
@@ -465,30 +519,59 @@ def run_rd(args):
     peak = peaks["bf16_tflops"]
     traffic = recorded_traffic("grouped_gemm_fwd", w.name)
 
-    # end to end through the C ABI with pinned host buffers
+    # End to end through the C ABI with pinned host buffers: every step copies its
+    # inputs (lhs, rhs, group_sizes) host -> device, runs the forward, and copies
+    # the output back.  Steps are pipelined over three streams with two device
+    # buffer sets: the upload of step i+1 and the download of step i-1 overlap
+    # the forward of step i.
     h_lhs = lhs.cpu().pin_memory()
     h_rhs = rhs.cpu().pin_memory()
     h_gs = gs.cpu().pin_memory()
-    h_out = torch.empty((w.m, w.n), dtype=torch.bfloat16).pin_memory()
-    d_lhs, d_rhs, d_gs = torch.empty_like(lhs), torch.empty_like(rhs), torch.empty_like(gs)
-    del lhs, rhs
+    h_out = [torch.empty((w.m, w.n), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    del lhs, rhs, out
     torch.cuda.empty_cache()
-
-    def e2e_step():
-        d_lhs.copy_(h_lhs, non_blocking=True)
-        d_rhs.copy_(h_rhs, non_blocking=True)
-        d_gs.copy_(h_gs, non_blocking=True)
-        rd.ragged_dot(d_lhs, d_rhs, d_gs, out=out, stream=stream)
-        h_out.copy_(out, non_blocking=True)
-
+    bufs = [(torch.empty((w.m, w.k), dtype=torch.bfloat16, device=device),
+             torch.empty((w.g_total, w.k, w.n), dtype=torch.bfloat16, device=device),
+             torch.empty((w.g_total,), dtype=torch.int32, device=device),
+             torch.empty((w.m, w.n), dtype=torch.bfloat16, device=device)) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     e2e_steps = max(3, min(args.steps, 10))
-    with torch.cuda.stream(stream):
-        _, e2e_ms = time_launches(e2e_step, e2e_steps, 2, stream)
-    e2e_ms = max_over_ranks(pg, e2e_ms, device)
+
+    def run_e2e(nsteps):
+        loaded = [torch.cuda.Event() for _ in range(nsteps)]
+        computed = [torch.cuda.Event() for _ in range(nsteps)]
+        stored = [torch.cuda.Event() for _ in range(nsteps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(s_in)
+        for i in range(nsteps):
+            d_lhs, d_rhs, d_gs, d_out = bufs[i % 2]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(computed[i - 2])      # buffer set free again
+                d_lhs.copy_(h_lhs, non_blocking=True)
+                d_rhs.copy_(h_rhs, non_blocking=True)
+                d_gs.copy_(h_gs, non_blocking=True)
+                loaded[i].record(s_in)
+            stream.wait_event(loaded[i])
+            if i >= 2:
+                stream.wait_event(stored[i - 2])          # output buffer downloaded
+            rd.ragged_dot(d_lhs, d_rhs, d_gs, out=d_out, stream=stream)
+            computed[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(computed[i])
+                h_out[i % 2].copy_(d_out, non_blocking=True)
+                stored[i].record(s_out)
+        s_out.wait_event(stored[nsteps - 1])
+        t1.record(s_out)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+
+    run_e2e(2)  # warm-up
+    e2e_ms = max_over_ranks(pg, run_e2e(e2e_steps), device)
     e2e_value = world * flops / (e2e_ms / e2e_steps * 1e-3) / 1e12
     h2d = h_lhs.numel() * 2 + h_rhs.numel() * 2 + h_gs.numel() * 4
-    d2h = h_out.numel() * 2
-    del d_lhs, d_rhs, h_out
+    d2h = h_out[0].numel() * 2
+    del bufs
     torch.cuda.empty_cache()
 
     ops = None
@@ -525,7 +608,8 @@ def run_rd(args):
                          "algorithmic_bytes": alg_bytes,
                          "kernel": "grouped_gemm_kernel<fwd>"},
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "pipelined": "upload i+1 / forward i / download i-1 on three streams"},
             "gpu_launches": args.steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
@@ -579,6 +663,16 @@ def run_profile(args):
             x = normal_bf16((w.m, w.k), 1.0, 40, device)
             dw = torch.empty((w.g_total, w.k, w.n), dtype=torch.bfloat16, device=device)
             fn = lambda: rd.trans_ragged_dot(x, do, gs, out=dw)
+    elif name == "packed_dx_glu_bwd":
+        w = workloads.packed_glu_fwd()
+        gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=device)
+        lim = torch.tensor([w.limit], dtype=torch.int32, device=device)
+        d_out = normal_bf16((w.m, 4096), 1.0, 35, device)
+        w_down = normal_bf16((w.g_local, 1024, 4096), 1.0 / 4096, 36, device)
+        fused2 = normal_bf16((w.m, 2048), 1.0, 37, device)
+        dfused2 = torch.empty_like(fused2)
+        fn = lambda: rd.ragged_dot_trans_rhs_glu_bwd(d_out, w_down, fused2, gs, w.group_offset, lim,
+                                                     dfused2)
     elif name == "unsort":
         w = workloads.packed_glu_fwd()
         lim = torch.tensor([w.limit], dtype=torch.int32, device=device)

@@ -28,7 +28,8 @@ enum GemmEpi : int {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue, warp 6 zero fill
+constexpr int kEpiWarps = 8;    // two epilogue warps per 32-lane quarter of the accumulator
+constexpr int kThreads = 384;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue, warp 10 zero fill
 constexpr int kTmemCols = 2 * kBN;  // two accumulators (double buffer)
 constexpr int kMaxGroups = 1024;
 

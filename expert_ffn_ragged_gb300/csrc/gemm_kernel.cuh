@@ -11,7 +11,7 @@
 //   dw       out[j]  = x[rows_j]^T @ y[rows_j]
 //   rows in [0, L) outside the local groups are +0, rows >= L untouched.
 //
-// How (persistent, 256 threads per CTA):
+// How (persistent, 384 threads per CTA):
 //   * every CTA reads group_sizes and *limit itself and builds the group
 //     boundaries (exclusive prefix clamped to L) and the per-group tile
 //     prefix in shared memory -- no workspace, no host round trip;
@@ -21,10 +21,11 @@
 //     band's lhs rows stay in L2 until every column panel has used them;
 //   * warp 0 (one lane) streams A/B blocks with TMA into a ring of
 //     128-byte-swizzled tiles; warp 1 issues tcgen05.mma into one of two
-//     TMEM accumulators; warps 2-5 drain the other accumulator with
+//     TMEM accumulators; warps 2-9 (two per TMEM lane quarter) drain the other
+//     accumulator with
 //     tcgen05.ld, round to bf16 (or apply the GLU) and store full 64-byte row
 //     segments through a small shared-memory transpose, with row masks;
-//     warp 6 has the bulk-copy engine write the zero rows of the forward/dx
+//     warp 10 has the bulk-copy engine write the zero rows of the forward/dx
 //     outputs from a zero block in shared memory;
 //   * PAIR=false: one CTA per SM computes a 128x256 tile (UMMA 128x256x16,
 //     4-stage ring of 48 KB).  PAIR=true: a cluster of two CTAs computes a
@@ -87,8 +88,7 @@ struct alignas(16) GemmShared {
   int32_t zero_hi;  // forward/dx: rows [zero_hi, L) are zero
   int32_t bound[kMaxGroups + 1];       // group boundaries, clamped to L
   int32_t tile_start[kMaxGroups + 1];  // first tile of each local group
-  uint4 epi[4][32 * 8];                // epilogue staging per warp: 32 rows x 128 bytes
-                                       // (two 64-byte halves for bf16 chunks)
+  uint4 epi[kEpiWarps][32 * 4];        // epilogue staging per warp: 32 rows x 64 bytes
   uint4 zeros[256];                    // 4 KB zero block, the source of the zero-fill copies
 };
 
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ptx::smem_addr(&sh.tfull[b]), 1);
-      ptx::mbar_init(ptx::smem_addr(&sh.tempty[b]), PAIR ? 8 : 4);
+      ptx::mbar_init(ptx::smem_addr(&sh.tempty[b]), PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     ptx::mbar_init(ptx::smem_addr(&sh.drain), 1);
     sh.abort_flag = 0;
@@ -547,16 +547,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
-    // Each warp owns one 32-lane quarter of the accumulator (32 tile rows).  A
-    // 32-column chunk is read from TMEM (thread = row), rounded to bf16 (or
-    // put through the GLU), transposed through a 2 KB XOR-swizzled staging
-    // buffer, and stored 8 rows x 64 contiguous bytes per instruction.
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // Eight warps, two per 32-lane quarter of the accumulator (32 tile rows);
+    // the two split the tile's 32-column chunks.  A chunk is read from TMEM
+    // (thread = row), rounded to bf16 (or put through the GLU forward or
+    // backward), transposed through a 2 KB XOR-swizzled staging buffer, and
+    // stored 8 rows x 64 contiguous bytes per instruction.
+    const int e = warp - 2;
+    const int q = warp & 3;      // TMEM lane quarter this warp may access
+    const int half = e >> 2;     // which half of the chunks
     constexpr int tile_w = GLU ? kBN / 2 : kBN;
+    constexpr int kChunks = tile_w / 32;
+    const int c_begin = half * (kChunks / 2), c_end = c_begin + kChunks / 2;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
-    uint4* stg = sh.epi[q];
+    uint4* stg = sh.epi[e];
     const uint32_t tempty_leader =
         PAIR ? ptx::map_to_rank(ptx::smem_addr(&sh.tempty[0]), 0) : 0u;
     const int sr = lane >> 2;      // row (within 8) this lane stores
@@ -576,16 +581,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // write the 16 packed words of this lane's row into the staging buffer, then
       // store the chunk's 32 rows x 32 columns to global memory
       // (col_off shifts the destination, e.g. to the d_up half of a fused row)
-      auto emit = [&](const uint32_t (&p)[16], int col, int col_off, uint4* buf) {
+      auto emit = [&](const uint32_t (&p)[16], int col, int col_off) {
 #pragma unroll
         for (int v = 0; v < 4; ++v)
-          buf[lane * 4 + (v ^ ((lane >> 1) & 3))] =
+          stg[lane * 4 + (v ^ ((lane >> 1) & 3))] =
               make_uint4(p[4 * v], p[4 * v + 1], p[4 * v + 2], p[4 * v + 3]);
         __syncwarp();
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
           const int rl = it * 8 + sr;
-          const uint4 val = buf[rl * 4 + (piece ^ ((rl >> 1) & 3))];
+          const uint4 val = stg[rl * 4 + (piece ^ ((rl >> 1) & 3))];
           const int row = wrow0 + rl;
           const int c = col + piece * 8;
           if (row >= lo && row < hi && c + 8 <= args.n_out)
@@ -593,25 +598,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       };
-      // f32 output of dw: 32 rows x 32 columns (128 bytes a row) per chunk, stored
-      // 4 rows x 128 contiguous bytes per instruction; the accumulating form adds
-      // the chunk to what the output already holds
-      auto emit_f32 = [&](const uint32_t (&v)[32], int col) {
-        uint4* buf = sh.epi[q];
+      // f32 output of dw, 16 columns (64 bytes a row) at a time through the same
+      // staging layout; the accumulating form adds them to what the output holds
+      auto emit_f32 = [&](const uint32_t* v16, int col) {
 #pragma unroll
-        for (int pc = 0; pc < 8; ++pc)
-          buf[lane * 8 + (pc ^ (lane & 7))] =
-              make_uint4(v[4 * pc], v[4 * pc + 1], v[4 * pc + 2], v[4 * pc + 3]);
+        for (int v = 0; v < 4; ++v)
+          stg[lane * 4 + (v ^ ((lane >> 1) & 3))] =
+              make_uint4(v16[4 * v], v16[4 * v + 1], v16[4 * v + 2], v16[4 * v + 3]);
         __syncwarp();
         float* outf = reinterpret_cast<float*>(args.out) +
                       static_cast<size_t>(tl.j) * args.m_out * args.ldo;
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int rl = it * 4 + (lane >> 3);
-          const int pc = lane & 7;
-          uint4 val = buf[rl * 8 + (pc ^ (rl & 7))];
+        for (int it = 0; it < 4; ++it) {
+          const int rl = it * 8 + sr;
+          uint4 val = stg[rl * 4 + (piece ^ ((rl >> 1) & 3))];
           const int row = wrow0 + rl;
-          const int c = col + pc * 4;
+          const int c = col + piece * 4;
           if (row < hi && c + 4 <= args.n_out) {
             uint4* dst = reinterpret_cast<uint4*>(outf + static_cast<size_t>(row) * args.ldo + c);
             if (EPI == kEpiF32Acc) {
@@ -627,17 +629,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       };
       if (tl.nkb == 0) {
-        if (F32OUT) {
-          if (EPI == kEpiF32) {  // an empty group's block is zero (accumulating: unchanged)
-            const uint32_t z[32] = {};
-            for (int c = 0; c < tile_w / 32; ++c) emit_f32(z, col0 + c * 32);
-          }
-          continue;
-        }
         const uint32_t z[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
-        for (int c = 0; c < tile_w / 32; ++c) {
-          emit(z, col0 + c * 32, 0, stg);
-          if (EPI == kEpiGluBwd) emit(z, col0 + c * 32, args.n_out, stg);
+        for (int c = c_begin; c < c_end; ++c) {
+          if (F32OUT) {
+            if (EPI == kEpiF32) {  // an empty group's block is zero (accumulating: unchanged)
+              emit_f32(z, col0 + c * 32);
+              emit_f32(z, col0 + c * 32 + 16);
+            }
+          } else {
+            emit(z, col0 + c * 32, 0);
+            if (EPI == kEpiGluBwd) emit(z, col0 + c * 32, args.n_out);
+          }
         }
         continue;
       }
@@ -650,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           sh.tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
       if (GLU) {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = c_begin; c < c_end; ++c) {
           uint32_t g[32], u[32], p[16];
           ptx::tmem_load_32cols(tbase + c * 32, g);
           ptx::tmem_load_32cols(tbase + kBN / 2 + c * 32, u);
@@ -659,37 +661,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             p[i] = pack_bf16x2(glu_fwd_f32(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
                                glu_fwd_f32(__uint_as_float(g[2 * i + 1]),
                                            __uint_as_float(u[2 * i + 1])));
-          emit(p, col0 + c * 32, 0, stg);
+          emit(p, col0 + c * 32, 0);
         }
       } else if (EPI == kEpiGluBwd) {
-        // dh (f32, this tile's accumulator) meets the saved gate / up of the same rows:
-        // both are staged through shared memory with coalesced loads, the backward of
-        // the GLU runs per element in f32, and [d_gate | d_up] leave through emit().
+        // dh (f32, this tile's accumulator) meets the saved gate / up of the same row:
+        // each thread reads its row's 32 gate and 32 up values, the backward of the
+        // GLU runs per element in f32, and [d_gate | d_up] leave through emit().
         const __nv_bfloat16* fused = reinterpret_cast<const __nv_bfloat16*>(args.aux);
-        uint4* stg2 = sh.epi[q] + 32 * 4;
+        const int row = wrow0 + lane;
+        const bool row_ok = row >= lo && row < hi;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = c_begin; c < c_end; ++c) {
           const int col = col0 + c * 32;
+          uint4 G[4], U[4];
+          const __nv_bfloat16* src = fused + static_cast<size_t>(row) * (2 * args.n_out) + col;
 #pragma unroll
-          for (int it = 0; it < 4; ++it) {
-            const int rl = it * 8 + sr;
-            const int row = wrow0 + rl;
-            const int cc = col + piece * 8;
-            if (row >= lo && row < hi && cc + 8 <= args.n_out) {
-              const __nv_bfloat16* src = fused + static_cast<size_t>(row) * (2 * args.n_out) + cc;
-              const int slot = rl * 4 + (piece ^ ((rl >> 1) & 3));
-              stg[slot] = __ldg(reinterpret_cast<const uint4*>(src));
-              stg2[slot] = __ldg(reinterpret_cast<const uint4*>(src + args.n_out));
+          for (int w4 = 0; w4 < 4; ++w4) {
+            if (row_ok && col + 8 * w4 + 8 <= args.n_out) {
+              G[w4] = __ldg(reinterpret_cast<const uint4*>(src) + w4);
+              U[w4] = __ldg(reinterpret_cast<const uint4*>(src + args.n_out) + w4);
+            } else {
+              G[w4] = make_uint4(0, 0, 0, 0);
+              U[w4] = make_uint4(0, 0, 0, 0);
             }
           }
           uint32_t v[32], pg[16], pu[16];
           ptx::tmem_load_32cols(tbase + c * 32, v);
-          __syncwarp();
 #pragma unroll
           for (int w4 = 0; w4 < 4; ++w4) {
-            const int slot = lane * 4 + (w4 ^ ((lane >> 1) & 3));
-            const uint4 G = stg[slot], U = stg2[slot];
-            const uint32_t gw[4] = {G.x, G.y, G.z, G.w}, uw[4] = {U.x, U.y, U.z, U.w};
+            const uint32_t gw[4] = {G[w4].x, G[w4].y, G[w4].z, G[w4].w};
+            const uint32_t uw[4] = {U[w4].x, U[w4].y, U[w4].z, U[w4].w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               float dg0, du0, dg1, du1;
@@ -700,26 +701,26 @@ __global__ void __launch_bounds__(kThreads, 1)
               pu[w4 * 4 + i] = bf16x2_neg_zero_to_pos(pack_bf16x2(du0, du1));
             }
           }
-          __syncwarp();
-          emit(pg, col, 0, stg);
-          emit(pu, col, args.n_out, stg2);
+          emit(pg, col, 0);
+          emit(pu, col, args.n_out);
         }
       } else if (F32OUT) {
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = c_begin; c < c_end; ++c) {
           uint32_t v[32];
           ptx::tmem_load_32cols(tbase + c * 32, v);
           emit_f32(v, col0 + c * 32);
+          emit_f32(v + 16, col0 + c * 32 + 16);
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = c_begin; c < c_end; ++c) {
           uint32_t v[32], p[16];
           ptx::tmem_load_32cols(tbase + c * 32, v);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             p[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          emit(p, col0 + c * 32, 0, stg);
+          emit(p, col0 + c * 32, 0);
         }
       }
       ptx::tc_fence_before();
@@ -733,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
-  } else if (OP != kOpDw && warp == 6) {
+  } else if (OP != kOpDw && warp == 2 + kEpiWarps) {
     // ------------------------------------------------------------ zero fill
     // Rows [0, zero_lo) and [zero_hi, L) are two contiguous byte ranges of the
     // output (its rows are contiguous).  Each CTA takes a contiguous 16-byte
