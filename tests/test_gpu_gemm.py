@@ -415,3 +415,54 @@ def test_cuda_graph_follows_device_group_sizes(rd_lib):
         E = 1e-3 * math.sqrt(k) * np.abs(a64).max() * np.abs(w64).max()
         ref, tol = glu_epilogue_tol(plain[:, :n], plain[:, n:], E)
         assert_close(_f64(h), ref, tol, f"graph replay sizes {sizes}")
+
+
+# ------------------------------------------------------------------ extremes
+def test_maximum_group_count(rd_lib):
+    """g_total = RD_MAX_GROUPS (1024), most groups empty, an offset shard of 300 groups."""
+    rng = np.random.default_rng(40)
+    g = rd_lib.MAX_GROUPS
+    sizes = np.zeros(g, np.int64)
+    live = rng.choice(g, 96, replace=False)
+    sizes[live] = rng.integers(1, 40, 96)
+    sizes = sizes.tolist()
+    m = int(sum(sizes)) + 17
+    run_fwd(rd_lib, m, 64, 256, sizes, off=400, gl=300, seed=40)
+    run_dx(rd_lib, m, 256, 64, sizes, off=100, gl=600, seed=41)
+    run_dw(rd_lib, m, 64, 256, sizes, off=500, gl=200, seed=42)
+
+
+def test_empty_inputs_are_no_ops(rd_lib):
+    """m = 0 enqueues nothing for the row outputs; dw of zero rows is all zeros."""
+    gs = _i32([0, 0])
+    e = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
+    rd_lib.ragged_dot(e, torch.zeros((2, 64, 64), dtype=torch.bfloat16, device=DEV), gs)
+    rd_lib.ragged_dot_trans_rhs(e, torch.zeros((2, 64, 64), dtype=torch.bfloat16, device=DEV), gs)
+    out = torch.full((2, 64, 64), 3.0, dtype=torch.bfloat16, device=DEV)
+    rd_lib.trans_ragged_dot(e, e, gs, out=out)
+    f32 = torch.full((2, 64, 64), 3.0, dtype=torch.float32, device=DEV)
+    rd_lib.trans_ragged_dot_f32(e, e, gs, out=f32, accumulate=True)
+    torch.cuda.synchronize()
+    assert bool((out == 0).all())                 # no rows: zeros
+    assert bool((f32 == 3.0).all())               # accumulating nothing leaves the buffer
+
+
+def test_limit_zero_writes_nothing_anywhere(rd_lib):
+    m, k, n = 512, 64, 256
+    rng = np.random.default_rng(43)
+    lhs = _normal(rng, (m, k)).to(DEV)
+    w = _normal(rng, (4, k, n), 1 / k).to(DEV)
+    fused = _normal(rng, (m, 2 * k)).to(DEV)
+    gs = _i32([100, 200, 100, 112])
+    zero = _i32([0])
+    outs = [_sentinel_buffer(m, n), _sentinel_buffer(m, n // 2), _sentinel_buffer(m, k),
+            _sentinel_buffer(m, 2 * k), _sentinel_buffer(m, k)]
+    rd_lib.ragged_dot(lhs, w, gs, limit=zero, out=outs[0][:m])
+    rd_lib.ragged_dot(lhs, w, gs, limit=zero, epilogue=rd_lib.EPI_SILU_GLU, out=outs[1][:m])
+    d_out = _normal(rng, (m, n)).to(DEV)
+    rd_lib.ragged_dot_trans_rhs(d_out, w, gs, limit=zero, out=outs[2][:m])
+    rd_lib.ragged_dot_trans_rhs_glu_bwd(d_out, w, fused, gs, limit=zero, out=outs[3][:m])
+    rd_lib.glu_fwd(fused, limit=zero, out=outs[4][:m])
+    torch.cuda.synchronize()
+    for o in outs:
+        assert bool((o.view(torch.int16) == SENT).all())
