@@ -56,16 +56,22 @@ def load_peaks():
 
 # ----------------------------------------------------------------- helpers
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    """nvidia-smi clock / throttle sampling around the timed region.
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Samples carry nvidia-smi's own timestamps; ``mark_start`` / ``mark_end``
+    bracket the timed region on the host clock and only the samples inside it
+    are summarised (all samples when the region is shorter than one period).
+    """
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 50):
+    def __init__(self, gpu_index: int, period_ms: int = 20):
         self.proc = None
         self.gpu = gpu_index
         self.period = period_ms
+        self.t_start = self.t_end = None
 
     def __enter__(self):
         try:
@@ -77,6 +83,12 @@ class ClockSampler:
             self.proc = None
         time.sleep(0.3)
         return self
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
 
     def __exit__(self, *exc):
         self.lines = []
@@ -92,26 +104,30 @@ class ClockSampler:
         return False
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        import datetime
+
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in getattr(self, "lines", []):
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, mx = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for name, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
-        # median under load: samples at the upper half of the observed range
-        hi = sorted(sm)[len(sm) // 2:]
-        return {"sm_mhz": statistics.median(hi), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+            active = {n for n, v in zip(names, parts[6:10]) if v.lower() == "active"}
+            rows.append((ts, sm, mx, active))
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [r for r in rows if self.t_start is not None and self.t_end is not None
+                  and self.t_start <= r[0] <= self.t_end]
+        use = inside if inside else rows
+        reasons = sorted(set().union(*[r[3] for r in use]))
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": use[0][2],
+                "reasons": reasons, "samples": len(use),
+                "window": "timed region" if inside else "whole sampling window"}
 
 
 def kernel_source_hash():
@@ -369,10 +385,9 @@ def run_ops(rd, device, stream, peaks):
 
 def ffn_sweep(rd, device, stream, peaks, tokens=(256, 1024, 4096, 16384)):
     """Up (GLU) + down projections of 128 experts (4096 -> 1536 -> 4096), top-8 routing."""
-    import numpy as np
     import torch
 
-    from workloads import normal_bf16, topk_counts
+    from workloads import expert_ffn, normal_bf16
 
     P = peaks["bf16_tflops"] * 1e12
     BW = peaks["hbm_gbs"] * 1e9
@@ -381,10 +396,10 @@ def ffn_sweep(rd, device, stream, peaks, tokens=(256, 1024, 4096, 16384)):
     down = normal_bf16((g, n // 2, k), 1.0 / (n // 2), 62, device)
     rows_out = []
     for t in tokens:
-        rng = np.random.default_rng(t)
-        logits = rng.standard_normal((t, g)) + rng.standard_normal(g)
-        sizes = topk_counts(logits, 8)
-        m = int(sizes.sum())
+        w = expert_ffn(t)
+        assert (w.g_total, w.k, w.n) == (g, k, n)
+        sizes = w.group_sizes
+        m = w.m
         lhs = normal_bf16((m, k), 1.0, 63, device)
         gs = torch.tensor(sizes, dtype=torch.int32, device=device)
         h = torch.empty((m, n // 2), dtype=torch.bfloat16, device=device)
@@ -508,7 +523,9 @@ def run_rd(args):
         if pg is not None:
             pg.barrier()
         with ClockSampler(local) as clk:
+            clk.mark_start()
             per, total_ms = time_launches(step, args.steps, 0, stream)
+            clk.mark_end()
         if pg is not None:
             pg.barrier()
     total_ms = max_over_ranks(pg, total_ms, device)

@@ -147,6 +147,22 @@ bool use_pair(int sms, int64_t m, int32_t g_total) {
   return m >= 512 * static_cast<int64_t>(g_total);
 }
 
+// m-tiles per band of the forward / dx tile order: the band's lhs rows stay in
+// L2 while the band sweeps every output column block.  4096 rows by default;
+// RD_BAND_ROWS overrides it (for measurements).
+int32_t band_tiles(bool pair) {
+  int64_t rows = 4096;
+  const char* v = getenv("RD_BAND_ROWS");
+  if (v != nullptr && *v != 0) {
+    char* end = nullptr;
+    const long long r = strtoll(v, &end, 10);
+    if (end != nullptr && *end == 0 && r > 0 && r < (1LL << 30)) rows = r;
+  }
+  const int64_t tile = pair ? 2 * kBM : kBM;
+  const int64_t t = rows / tile;
+  return static_cast<int32_t>(t < 1 ? 1 : t);
+}
+
 int pair_grid(int sms, int64_t pair_tiles_upper_bound) {
   return 2 * grid_for(sms / 2, pair_tiles_upper_bound);
 }
@@ -212,6 +228,7 @@ extern "C" rd_status rd_ragged_dot(const void* lhs, const void* rhs, void* out, 
   a.dw_m_tiles = 0;
   a.timeout_ns = wait_timeout_ns();
   const bool pair = use_pair(sms, m, g_total);
+  a.band_tiles = band_tiles(pair);
   const int grid = pair ? pair_grid(sms, ((m + 2 * kBM - 1) / (2 * kBM) + g_local) * a.n_tiles)
                         : grid_for(sms, ((m + kBM - 1) / kBM + g_local) * a.n_tiles);
   return launch_gemm_fwd(glu, pair, ta, tb, a, grid, reinterpret_cast<cudaStream_t>(stream)) ==
@@ -276,6 +293,7 @@ rd_status trans_rhs_impl(const void* lhs, const void* rhs, const void* fused, vo
   a.group_offset = group_offset;
   a.g_local = g_local;
   a.n_tiles = static_cast<int32_t>((k + kBN - 1) / kBN);
+  a.band_tiles = band_tiles(pair);
   a.timeout_ns = wait_timeout_ns();
   const int grid = pair ? pair_grid(sms, ((m + 2 * kBM - 1) / (2 * kBM) + g_local) * a.n_tiles)
                         : grid_for(sms, ((m + kBM - 1) / kBM + g_local) * a.n_tiles);

@@ -51,6 +51,7 @@ struct GemmArgs {
   int32_t glu_f;               // fwd with GLU: first column of the up half in rhs (= n / 2)
   int32_t n_tiles;             // output column tiles
   int32_t dw_m_tiles;          // dw: 128-row tiles of each weight block
+  int32_t band_tiles;          // fwd/dx: m-tiles per band of the tile order (lhs rows kept in L2)
   uint64_t timeout_ns;         // bound of every wait inside the kernel
 };
 

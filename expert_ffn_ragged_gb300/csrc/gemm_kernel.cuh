@@ -16,7 +16,7 @@
 //     boundaries (exclusive prefix clamped to L) and the per-group tile
 //     prefix in shared memory -- no workspace, no host round trip;
 //   * tiles are handed out by static striding over (group, band, n-tile,
-//     m-tile): within a band of 4096 rows the m-tiles run fastest, so the CTAs
+//     m-tile): within a band of rows (4096 by default) the m-tiles run fastest, so the CTAs
 //     working at one time share each rhs column panel through L2 and the
 //     band's lhs rows stay in L2 until every column panel has used them;
 //   * warp 0 (one lane) streams A/B blocks with TMA into a ring of
@@ -37,8 +37,8 @@
 //   * the last m-tile of a group is loaded from row (end - tile rows) so no
 //     row at or past the group end -- hence none at or past L -- is read; it
 //     stores only the rows it owns.  dw uses the same shift on its row (K)
-//     blocks, skips whole 16-row K steps before the group and zeroes, in
-//     shared memory, the rows of the straddling step (NaN-safe);
+//     blocks, skips whole 16-row K steps before the group and has warp 10
+//     zero, in shared memory, the rows of the straddling step (NaN-safe);
 //   * every wait is bounded; on expiry the CTA unwinds, drains its TMA and
 //     MMA work, frees TMEM and reports RD_STATUS_TIMEOUT.
 #pragma once
@@ -58,8 +58,6 @@ namespace rd {
 // still in flight then completes within microseconds.
 constexpr uint64_t kDrainNs = 1000000000ull;
 constexpr uint64_t kGraceNs = 200000ull;
-// rows of lhs kept hot in L2 while a band of tiles sweeps the output columns
-constexpr int kBandRows = 4096;
 
 template <bool PAIR>
 struct TileCfg {
@@ -76,7 +74,8 @@ struct alignas(16) GemmShared {
   static constexpr int S = TileCfg<PAIR>::kStagesN;
   uint64_t full[S];
   uint64_t empty[S];
-  uint64_t pready[S];  // pair dw: the odd CTA's zeroed edge block is ready
+  uint64_t efull[S];   // dw: this CTA's copy of an edge block landed (edge fills only)
+  uint64_t pready[S];  // dw: the edge rows of this stage are zeroed (in a pair: in both CTAs)
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -207,10 +206,10 @@ __device__ __forceinline__ Tile decode_tile(const GemmShared<PAIR>& sh, const Ge
     const int u = t - sh.tile_start[lo];
     tl.rs = sh.bound[a.group_offset + lo];
     tl.re = sh.bound[a.group_offset + lo + 1];
-    // Bands of kBandRows rows: within a band the m-tiles run fastest and the
+    // Bands of band_tiles m-tiles: within a band the m-tiles run fastest and the
     // band sweeps every n-tile before the next band starts, so the band's lhs
     // rows stay in L2 while each rhs column panel is read once per band.
-    constexpr int kBand = kBandRows / TM;
+    const int kBand = a.band_tiles;
     const int mt = (tl.re - tl.rs + TM - 1) / TM;
     const int band = u / (kBand * a.n_tiles);
     const int rem = u - band * kBand * a.n_tiles;
@@ -288,7 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(ptx::smem_addr(&sh.full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&sh.empty[s]), 1);
-      ptx::mbar_init(ptx::smem_addr(&sh.pready[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&sh.efull[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&sh.pready[s]), PAIR ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(ptx::smem_addr(&sh.tfull[b]), 1);
@@ -326,6 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t pend_mask = 0, pend_par = 0;  // fills whose consumption is not yet seen
+      uint32_t pend_edge = 0, pend_cpar = 0;  // ... their barrier (edge or not) and its parity
+      uint32_t fpar = 0, epar = 0;            // per-slot parities of full / efull
       bool ok = true;
       for (int t = unit; t < total && ok; t += units) {
         const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
@@ -339,16 +341,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb_local = ptx::smem_addr(&sh.full[stage]);
           const uint32_t a_dst = ptx::smem_addr(sA + stage * Cfg::kStageA);
           const uint32_t b_dst = ptx::smem_addr(sB + stage * Cfg::kStageB);
-          if (PAIR && OP == kOpDw) {
-            // The last block of a group whose start straddles a 16-row K step is zeroed
-            // in each CTA before the MMA: the odd CTA's copy then counts on its own
-            // barrier (its warp 1 zeroes and signals), the even CTA expects only its own.
+          // dw: the last block of a group whose start straddles a 16-row K step must be
+          // zeroed in each CTA before the MMA reads it.  Its copy counts on this CTA's
+          // own edge barrier (efull), which only edge blocks use; the edge warp waits
+          // there, zeroes, and signals the MMA.
+          bool edge = false;
+          if (OP == kOpDw) {
             int z0, z1;
             dw_edge(tl, kb, z0, z1);
-            const bool edge = z1 > z0;
-            const uint32_t fb = edge ? fb_local : ptx::map_to_rank(fb_local, 0);
-            if (rank == 0 || edge)
-              ptx::mbar_arrive_expect_tx(fb_local, (edge ? 1 : 2) * Cfg::kStageBytes);
+            edge = z1 > z0;
+          }
+          const uint32_t eb_local = ptx::smem_addr(&sh.efull[stage]);
+          if (PAIR && OP == kOpDw) {
+            const uint32_t fb = edge ? eb_local : ptx::map_to_rank(fb_local, 0);
+            if (edge) ptx::mbar_arrive_expect_tx(eb_local, Cfg::kStageBytes);
+            else if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, 2 * Cfg::kStageBytes);
             const int row0 = (kb == tl.nkb - 1) ? tl.re - kBK : tl.rs + kb * kBK;
             const int ka = tl.m_idx * TM + static_cast<int>(rank) * kBM;
             const int nb = tl.n_idx * kBN + static_cast<int>(rank) * (kBN / 2);
@@ -377,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     tl.n_idx * kBN + static_cast<int>(rank) * (kBN / 2), tl.j);
             }
           } else {
-            const uint32_t fb = fb_local;
+            const uint32_t fb = edge ? eb_local : fb_local;
             ptx::mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
             if (OP == kOpFwd) {
               ptx::tma_load_2d(a_dst, &tmap_a, fb, kb * kBK, tl.row_load);
@@ -402,6 +409,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           pend_mask |= 1u << stage;
           pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+          // parity of the barrier this fill completes (full: non-edge fills, efull: edge fills)
+          const uint32_t cnt_par = edge ? ((epar >> stage) & 1u) : ((fpar >> stage) & 1u);
+          pend_edge = (pend_edge & ~(1u << stage)) | ((edge ? 1u : 0u) << stage);
+          pend_cpar = (pend_cpar & ~(1u << stage)) | (cnt_par << stage);
+          if (edge) epar ^= 1u << stage; else fpar ^= 1u << stage;
           if (++stage == S) {
             stage = 0;
             phase ^= 1;
@@ -418,13 +430,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(pend_mask & (1u << s))) continue;
         const uint32_t par = (pend_par >> s) & 1u;
         if (*abort_flag) {
-          if (!PAIR || rank == 0)
-            ptx::mbar_wait_bounded(ptx::smem_addr(&sh.full[s]), par, &no_abort, kDrainNs);
+          const bool e = (pend_edge >> s) & 1u;
+          const uint32_t cp = (pend_cpar >> s) & 1u;
+          if (e)
+            ptx::mbar_wait_bounded(ptx::smem_addr(&sh.efull[s]), cp, &no_abort, kDrainNs);
+          else if (!PAIR || rank == 0)
+            ptx::mbar_wait_bounded(ptx::smem_addr(&sh.full[s]), cp, &no_abort, kDrainNs);
         } else {
           ptx::mbar_wait_bounded(ptx::smem_addr(&sh.empty[s]), par, &no_abort, kDrainNs);
         }
       }
-      if (PAIR && rank != 0 && *abort_flag && pend_mask != 0) {
+      if (PAIR && rank != 0 && *abort_flag && (pend_mask & ~pend_edge) != 0) {
         const uint64_t t0 = ptx::global_timer_ns();
         while (ptx::global_timer_ns() - t0 < kGraceNs) __nanosleep(1000);
       }
@@ -440,7 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      uint32_t pready_par = 0;
+      uint32_t pready_par = 0;  // per-slot parity of pready (edge blocks)
+      uint32_t full_par = 0;    // per-slot parity of full (every other block)
       bool ok = true;
       for (int t = unit; t < total && ok; t += units) {
         const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
@@ -452,31 +469,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const uint32_t d_tmem = sh.tmem_base + static_cast<uint32_t>(acc * kBN);
         for (int kb = 0; kb < tl.nkb; ++kb) {
-          ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.full[stage]), phase, abort_flag,
-                                              tlimit);
+          int kk0 = 0;  // first 16-deep K step issued for this block
+          bool edge = false;
+          if (OP == kOpDw) {
+            int z0, z1;
+            kk0 = dw_edge(tl, kb, z0, z1);
+            edge = z1 > z0;
+          }
+          if (edge) {
+            // rows of a neighbouring group (or a NaN) must not enter the sum: the
+            // straddling rows of an edge block are zeroed by the edge warp of each CTA,
+            // which signals pready once its part is done (its copy has landed by then)
+            const uint32_t pb = ptx::smem_addr(&sh.pready[stage]);
+            const uint32_t par = (pready_par >> stage) & 1u;
+            ok = PAIR ? ptx::mbar_wait_bounded_cluster(pb, par, abort_flag, tlimit)
+                      : ptx::mbar_wait_bounded(pb, par, abort_flag, tlimit);
+            pready_par ^= 1u << stage;
+          } else {
+            ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.full[stage]), (full_par >> stage) & 1u,
+                                        abort_flag, tlimit);
+            full_par ^= 1u << stage;
+          }
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) break;
           ptx::tc_fence_after();
           uint8_t* a_st = sA + stage * Cfg::kStageA;
           uint8_t* b_st = sB + stage * Cfg::kStageB;
-          int kk0 = 0;  // first 16-deep K step issued for this block
-          if (OP == kOpDw) {
-            // rows of a neighbouring group (or a NaN) must not enter the sum
-            int z0, z1;
-            kk0 = dw_edge(tl, kb, z0, z1);
-            if (z1 > z0) {
-              dw_zero_rows<2, Cfg::kBCols / 64>(a_st, b_st, z0, z1, lane);
-              __syncwarp();
-              if (PAIR) {
-                // the odd CTA has zeroed the same rows of its half
-                ok = ptx::mbar_wait_bounded_cluster(ptx::smem_addr(&sh.pready[stage]),
-                                                    (pready_par >> stage) & 1u, abort_flag, tlimit);
-                pready_par ^= 1u << stage;
-                ok = __all_sync(0xFFFFFFFFu, ok);
-                if (!ok) break;
-              }
-            }
-          }
           if (lane == 0) {
             const uint32_t a_addr = ptx::smem_addr(a_st);
             const uint32_t b_addr = ptx::smem_addr(b_st);
@@ -518,33 +536,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_wait_bounded(ptx::smem_addr(&sh.drain), 0, &no_abort, kDrainNs);
         }
         __syncwarp();
-      }
-    } else if (OP == kOpDw) {
-      // odd CTA of a dw pair: zero the straddling rows of each edge block once its own
-      // copy has landed, then tell the even CTA, whose MMA reads this CTA's half
-      int stage = 0;
-      uint32_t lpar = 0;  // phase of this CTA's own full barrier, per stage
-      const uint32_t pready0 = ptx::map_to_rank(ptx::smem_addr(&sh.pready[0]), 0);
-      bool ok = true;
-      for (int t = unit; t < total && ok; t += units) {
-        const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
-        for (int kb = 0; kb < tl.nkb; ++kb) {
-          int z0, z1;
-          dw_edge(tl, kb, z0, z1);
-          if (z1 > z0) {
-            ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.full[stage]), (lpar >> stage) & 1u,
-                                        abort_flag, tlimit);
-            lpar ^= 1u << stage;
-            ok = __all_sync(0xFFFFFFFFu, ok);
-            if (!ok) break;
-            dw_zero_rows<2, Cfg::kBCols / 64>(sA + stage * Cfg::kStageA, sB + stage * Cfg::kStageB,
-                                             z0, z1, lane);
-            __syncwarp();
-            if (lane == 0)
-              ptx::mbar_arrive_cluster(pready0 + static_cast<uint32_t>(stage * sizeof(uint64_t)));
-          }
-          if (++stage == S) stage = 0;
-        }
       }
     }
   } else if (warp < 2 + kEpiWarps) {
@@ -734,6 +725,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+  } else if (OP == kOpDw && warp == 2 + kEpiWarps) {
+    // ------------------------------------------------------------ dw edge rows
+    // For each edge block (the last K block of a group, whose first rows precede
+    // the group), wait for this CTA's own copy, zero the rows of the straddling
+    // 16-row step in both operands, and signal the MMA (in a pair: the even
+    // CTA's barrier, which expects both CTAs).  The producer runs ahead of the
+    // MMA, so this usually finishes before the MMA reaches the block.
+    int stage = 0;
+    uint32_t lpar = 0;  // per-slot parity of this CTA's efull barrier
+    const uint32_t pready0 = PAIR ? ptx::map_to_rank(ptx::smem_addr(&sh.pready[0]), 0)
+                                  : ptx::smem_addr(&sh.pready[0]);
+    bool ok = true;
+    for (int t = unit; t < total && ok; t += units) {
+      const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
+      for (int kb = 0; kb < tl.nkb; ++kb) {
+        int z0, z1;
+        dw_edge(tl, kb, z0, z1);
+        if (z1 > z0) {
+          ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.efull[stage]), (lpar >> stage) & 1u,
+                                      abort_flag, tlimit);
+          lpar ^= 1u << stage;
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (!ok) break;
+          dw_zero_rows<2, Cfg::kBCols / 64>(sA + stage * Cfg::kStageA, sB + stage * Cfg::kStageB,
+                                           z0, z1, lane);
+          __syncwarp();
+          if (lane == 0) {
+            const uint32_t pb = pready0 + static_cast<uint32_t>(stage * sizeof(uint64_t));
+            if (PAIR) ptx::mbar_arrive_cluster(pb);
+            else ptx::mbar_arrive(pb);
+          }
+        }
+        if (++stage == S) stage = 0;
+      }
+    }
   } else if (OP != kOpDw && warp == 2 + kEpiWarps) {
     // ------------------------------------------------------------ zero fill
     // Rows [0, zero_lo) and [zero_hi, L) are two contiguous byte ranges of the
@@ -783,13 +809,16 @@ template <int OP, int EPI, bool PAIR>
 cudaError_t launch_gemm_impl(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                              const GemmArgs& args, int grid, cudaStream_t stream) {
   constexpr size_t smem = gemm_smem_bytes_t<PAIR>();
-  static bool attr_set = false;
-  if (!attr_set) {
+  // the shared-memory size attribute is set once per device (it is per-device state)
+  static bool attr_set[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
     const cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<OP, EPI, PAIR>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   if (!PAIR) {
     grouped_gemm_kernel<OP, EPI, PAIR><<<grid, kThreads, smem, stream>>>(tmap_a, tmap_b, args);
@@ -810,8 +839,6 @@ cudaError_t launch_gemm_impl(const CUtensorMap& tmap_a, const CUtensorMap& tmap_
   // a CTA pair must sit in one GPC, so fewer than (#SMs / 2) pairs may fit.  The
   // limit is queried once per device (it depends only on the kernel and the GPU).
   static int max_clusters[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (max_clusters[dev] == 0) {
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     int n = 0;

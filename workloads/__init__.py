@@ -29,6 +29,7 @@ __all__ = [
     "packed_glu_fwd",
     "backward_pair",
     "decode_fwd",
+    "expert_ffn",
     "normal_bf16",
     "normal_bf16_np",
     "random_sizes",
@@ -197,6 +198,21 @@ def decode_fwd(skewed: bool = True) -> Workload:
     tag = "skewed" if skewed else "uniform"
     return Workload(f"decode_{tag}_2048x4096x1536_g128", 2048, 4096, 1536, 128, sizes,
                     glu=True, lhs_var=1.0, rhs_var=1.0 / 4096, seed=5)
+
+
+def expert_ffn(tokens: int) -> Workload:
+    """Expert FFN forward at a batch of ``tokens`` tokens, top-8 of 128 experts.
+
+    The same layer as ``decode_fwd`` (up rhs [128,4096,1536] with the GLU
+    epilogue, down rhs [128,768,4096]) at larger batches, from weight-bound
+    (a few hundred tokens) to compute-bound (tens of thousands): the router
+    logits are N(0,1) plus a per-expert bias N(0,1), seeded by ``tokens``.
+    """
+    rng = np.random.default_rng(tokens)
+    logits = rng.standard_normal((tokens, 128)) + rng.standard_normal(128)
+    sizes = topk_counts(logits, 8)
+    return Workload(f"expert_ffn_{tokens}tok_top8_g128", int(sizes.sum()), 4096, 1536, 128,
+                    sizes, glu=True, lhs_var=1.0, rhs_var=1.0 / 4096, seed=tokens)
 
 
 WORKLOADS = {
