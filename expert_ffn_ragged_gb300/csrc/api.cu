@@ -350,20 +350,42 @@ rd_status trans_ragged_impl(const void* x, const void* y, void* out, int64_t m, 
   if ((st = current_device(&sms)) != RD_OK) return st;
   if (k == 0 || n == 0) return RD_OK;
 
+  const bool pair = use_pair(sms, m, g_total);
+  // Both operands are MN-major (the token rows are the contraction).  When a
+  // width is a multiple of 64 its map is 3-D, (64 columns, rows, 64-column
+  // chunks), so that one box brings all the chunks of a stage (the producer
+  // issues half as many copies); otherwise one 2-D box per 64 columns, whose
+  // zero fill covers the columns past the width.
+  const bool a_chunked = k % 64 == 0, b_chunked = n % 64 == 0;
   CUtensorMap ta = {}, tb = {};
   if (m > 0) {
-    const uint64_t da[2] = {static_cast<uint64_t>(k), static_cast<uint64_t>(m)};
-    const uint64_t sa[1] = {static_cast<uint64_t>(k) * 2};
-    const uint32_t ba[2] = {64, kBK};
-    if ((st = encode(&ta, x, 2, da, sa, ba)) != RD_OK) return st;
-    const uint64_t db[2] = {static_cast<uint64_t>(n), static_cast<uint64_t>(m)};
-    const uint64_t sb[1] = {static_cast<uint64_t>(n) * 2};
-    const uint32_t bb[2] = {64, kBK};
-    if ((st = encode(&tb, y, 2, db, sb, bb)) != RD_OK) return st;
+    if (a_chunked) {
+      const uint64_t da[3] = {64, static_cast<uint64_t>(m), static_cast<uint64_t>(k / 64)};
+      const uint64_t sa[2] = {static_cast<uint64_t>(k) * 2, 128};
+      const uint32_t ba[3] = {64, kBK, kBM / 64};
+      if ((st = encode(&ta, x, 3, da, sa, ba)) != RD_OK) return st;
+    } else {
+      const uint64_t da[2] = {static_cast<uint64_t>(k), static_cast<uint64_t>(m)};
+      const uint64_t sa[1] = {static_cast<uint64_t>(k) * 2};
+      const uint32_t ba[2] = {64, kBK};
+      if ((st = encode(&ta, x, 2, da, sa, ba)) != RD_OK) return st;
+    }
+    if (b_chunked) {
+      const uint64_t db[3] = {64, static_cast<uint64_t>(m), static_cast<uint64_t>(n / 64)};
+      const uint64_t sb[2] = {static_cast<uint64_t>(n) * 2, 128};
+      const uint32_t bb[3] = {64, kBK, static_cast<uint32_t>((pair ? kBN / 2 : kBN) / 64)};
+      if ((st = encode(&tb, y, 3, db, sb, bb)) != RD_OK) return st;
+    } else {
+      const uint64_t db[2] = {static_cast<uint64_t>(n), static_cast<uint64_t>(m)};
+      const uint64_t sb[1] = {static_cast<uint64_t>(n) * 2};
+      const uint32_t bb[2] = {64, kBK};
+      if ((st = encode(&tb, y, 2, db, sb, bb)) != RD_OK) return st;
+    }
   }
-  const bool pair = use_pair(sms, m, g_total);
   const int tile_rows = pair ? 2 * kBM : kBM;  // rows of dw[j] (the k axis) per tile
   GemmArgs a = {};
+  a.a_chunked = a_chunked ? 1 : 0;
+  a.b_chunked = b_chunked ? 1 : 0;
   a.group_sizes = group_sizes;
   a.limit = limit;
   a.status = status;

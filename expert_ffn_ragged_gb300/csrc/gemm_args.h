@@ -52,6 +52,8 @@ struct GemmArgs {
   int32_t n_tiles;             // output column tiles
   int32_t dw_m_tiles;          // dw: 128-row tiles of each weight block
   int32_t band_tiles;          // fwd/dx: m-tiles per band of the tile order (lhs rows kept in L2)
+  int32_t a_chunked;           // dw: tmap_a is (64, rows, width / 64): one box per stage
+  int32_t b_chunked;           // dw: tmap_b likewise (else 2-D maps, one box per 64 columns)
   uint64_t timeout_ns;         // bound of every wait inside the kernel
 };
 

@@ -85,6 +85,7 @@ struct alignas(16) GemmShared {
   int32_t total_tiles;
   int32_t zero_lo;  // forward/dx: rows [0, zero_lo) are zero
   int32_t zero_hi;  // forward/dx: rows [zero_hi, L) are zero
+  int32_t epi_tiles;  // tiles whose accumulator the epilogue has taken (paces the zero fill)
   int32_t bound[kMaxGroups + 1];       // group boundaries, clamped to L
   int32_t tile_start[kMaxGroups + 1];  // first tile of each local group
   uint4 epi[kEpiWarps][32 * 4];        // epilogue staging per warp: 32 rows x 64 bytes
@@ -296,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(ptx::smem_addr(&sh.drain), 1);
     sh.abort_flag = 0;
+    sh.epi_tiles = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0 && args.kc > 0) {
@@ -359,10 +361,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row0 = (kb == tl.nkb - 1) ? tl.re - kBK : tl.rs + kb * kBK;
             const int ka = tl.m_idx * TM + static_cast<int>(rank) * kBM;
             const int nb = tl.n_idx * kBN + static_cast<int>(rank) * (kBN / 2);
+            // a chunked map lands its 64-column chunks 8 KB apart, as separate boxes would
+            if (args.a_chunked) {
+              ptx::tma_load_3d_pair(a_dst, &tmap_a, fb, 0, row0, ka / 64);
+            } else {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              ptx::tma_load_2d_pair(a_dst + c * (kBK * 128), &tmap_a, fb, ka + c * 64, row0);
-              ptx::tma_load_2d_pair(b_dst + c * (kBK * 128), &tmap_b, fb, nb + c * 64, row0);
+              for (int c = 0; c < 2; ++c)
+                ptx::tma_load_2d_pair(a_dst + c * (kBK * 128), &tmap_a, fb, ka + c * 64, row0);
+            }
+            if (args.b_chunked) {
+              ptx::tma_load_3d_pair(b_dst, &tmap_b, fb, 0, row0, nb / 64);
+            } else {
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+                ptx::tma_load_2d_pair(b_dst + c * (kBK * 128), &tmap_b, fb, nb + c * 64, row0);
             }
           } else if (PAIR) {
             // Both CTAs' bytes are counted on the even CTA's barrier, which expects them
@@ -399,12 +411,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::tma_load_3d(b_dst, &tmap_b, fb, kb * kBK, tl.n_idx * kBN, tl.j);
             } else {
               const int row0 = (kb == tl.nkb - 1) ? tl.re - kBK : tl.rs + kb * kBK;
+              if (args.a_chunked) {
+                ptx::tma_load_3d(a_dst, &tmap_a, fb, 0, row0, tl.m_idx * (kBM / 64));
+              } else {
 #pragma unroll
-              for (int c = 0; c < 2; ++c)
-                ptx::tma_load_2d(a_dst + c * (kBK * 128), &tmap_a, fb, tl.m_idx * kBM + c * 64, row0);
+                for (int c = 0; c < 2; ++c)
+                  ptx::tma_load_2d(a_dst + c * (kBK * 128), &tmap_a, fb, tl.m_idx * kBM + c * 64, row0);
+              }
+              if (args.b_chunked) {
+                ptx::tma_load_3d(b_dst, &tmap_b, fb, 0, row0, tl.n_idx * (kBN / 64));
+              } else {
 #pragma unroll
-              for (int c = 0; c < 4; ++c)
-                ptx::tma_load_2d(b_dst + c * (kBK * 128), &tmap_b, fb, tl.n_idx * kBN + c * 64, row0);
+                for (int c = 0; c < 4; ++c)
+                  ptx::tma_load_2d(b_dst + c * (kBK * 128), &tmap_b, fb, tl.n_idx * kBN + c * 64, row0);
+              }
             }
           }
           pend_mask |= 1u << stage;
@@ -559,6 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int piece = lane & 3;    // 16-byte piece of the row's 64 bytes
     int acc = 0;
     uint32_t acc_phase = 0;
+    int tiles_taken = 0;
     for (int t = unit; t < total; t += units) {
       const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
       // first row of this warp's 32 rows and the rows it may write: [lo, hi)
@@ -620,6 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       };
       if (tl.nkb == 0) {
+        if (e == 0 && lane == 0) *reinterpret_cast<volatile int32_t*>(&sh.epi_tiles) = ++tiles_taken;
         const uint32_t z[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
         for (int c = c_begin; c < c_end; ++c) {
           if (F32OUT) {
@@ -638,6 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        tlimit);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
+      if (e == 0 && lane == 0) *reinterpret_cast<volatile int32_t*>(&sh.epi_tiles) = ++tiles_taken;
       ptx::tc_fence_after();
       const uint32_t tbase =
           sh.tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
@@ -765,7 +788,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Rows [0, zero_lo) and [zero_hi, L) are two contiguous byte ranges of the
     // output (its rows are contiguous).  Each CTA takes a contiguous 16-byte
     // aligned share of their concatenation and has the bulk-copy engine write it
-    // from a 4 KB zero block in shared memory.
+    // from a 4 KB zero block in shared memory.  The share goes out in slices,
+    // one more each time the epilogue takes a tile's accumulator, and all of it
+    // before the CTA's last tile: the writes then spread over the run instead
+    // of meeting the first tiles' operand reads in HBM in one burst.
     for (int i = lane; i < 256; i += 32) sh.zeros[i] = make_uint4(0, 0, 0, 0);
     ptx::fence_proxy_async_smem();
     __syncwarp();
@@ -774,21 +800,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t lo_bytes = static_cast<uint64_t>(sh.zero_lo) * row_bytes;
       const uint64_t z_bytes = lo_bytes + static_cast<uint64_t>(sh.L - sh.zero_hi) * row_bytes;
       const uint64_t units16 = z_bytes / 16;
-      const uint64_t b0 = units16 * blockIdx.x / gridDim.x * 16;
-      const uint64_t b1 = units16 * (blockIdx.x + 1) / gridDim.x * 16;
+      const uint64_t u0 = units16 * blockIdx.x / gridDim.x;
+      const uint64_t u1 = units16 * (blockIdx.x + 1) / gridDim.x;
+      const int my_tiles = unit < total ? (total - 1 - unit) / units + 1 : 0;
+      const int slices = my_tiles > 2 ? my_tiles - 1 : 1;
+      const volatile int32_t* taken = &sh.epi_tiles;
       char* base = reinterpret_cast<char*>(args.out);
       const uint32_t src = ptx::smem_addr(sh.zeros);
-      uint64_t b = b0;
-      while (b < b1) {
-        const bool low = b < lo_bytes;
-        const uint64_t seg_end = low ? lo_bytes : z_bytes;
-        const uint64_t addr = low ? b : static_cast<uint64_t>(sh.zero_hi) * row_bytes + (b - lo_bytes);
-        uint64_t len = (b1 < seg_end ? b1 : seg_end) - b;
-        if (len > 4096) len = 4096;
-        ptx::bulk_copy_s2g(base + addr, src, static_cast<uint32_t>(len));
-        b += len;
+#pragma unroll 1
+      for (int j = 0; j < slices && u1 > u0; ++j) {
+        if (j > 0 && *taken < j) {
+          // pacing only: give up (and unwind with the CTA) like any other wait
+          const uint64_t t0 = ptx::global_timer_ns();
+          while (*taken < j && !*abort_flag) {
+            if (ptx::global_timer_ns() - t0 > tlimit) {
+              *abort_flag = 1;
+              break;
+            }
+            __nanosleep(500);
+          }
+          if (*abort_flag) break;
+        }
+        uint64_t b = (u0 + (u1 - u0) * j / slices) * 16;
+        const uint64_t b1 = (u0 + (u1 - u0) * (j + 1) / slices) * 16;
+        while (b < b1) {
+          const bool low = b < lo_bytes;
+          const uint64_t seg_end = low ? lo_bytes : z_bytes;
+          const uint64_t addr = low ? b : static_cast<uint64_t>(sh.zero_hi) * row_bytes + (b - lo_bytes);
+          uint64_t len = (b1 < seg_end ? b1 : seg_end) - b;
+          if (len > 4096) len = 4096;
+          ptx::bulk_copy_s2g(base + addr, src, static_cast<uint32_t>(len));
+          b += len;
+        }
+        ptx::bulk_commit();
       }
-      ptx::bulk_commit();
       ptx::bulk_wait_read_all();
     }
   }

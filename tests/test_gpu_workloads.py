@@ -200,3 +200,70 @@ def test_decode_pair_in_one_graph(rd_lib, skewed):
         assert_close(got_h[lo:hi], ref, tol, f"decode up group {j}")
         ref = h64[lo:hi] @ _f64(down[j][:, ocidx])
         assert_close(got_o[lo:hi], ref, gemm_tol(ref, F, Eo_amax, Eo_bmax), f"decode down group {j}")
+
+
+@pytest.mark.parametrize("tokens", [4096, 16384])
+def test_expert_ffn_chain_in_one_graph(rd_lib, tokens):
+    """Up projection with the GLU epilogue feeding the down projection, one CUDA graph.
+
+    The expert FFN forward at batches between weight-bound and compute-bound
+    (4096 and 16384 tokens, top-8 of 128 experts).  The down call consumes the
+    h the up call wrote inside the same graph; both outputs are checked on
+    sampled rows and columns of every live group (h against the float64 GLU of
+    the up GEMM, the output against the float64 down GEMM of that h), and on
+    the device every row of both must have been written.
+    """
+    from workloads import expert_ffn, normal_bf16
+
+    w = expert_ffn(tokens)
+    F = w.n // 2
+    lhs = normal_bf16((w.m, w.k), w.lhs_var, 63, DEV)
+    up = normal_bf16((w.g_total, w.k, w.n), w.rhs_var, 61, DEV)
+    down = normal_bf16((w.g_total, F, w.k), 1.0 / F, 62, DEV)
+    gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=DEV)
+    h = torch.empty((w.m, F), dtype=torch.bfloat16, device=DEV)
+    o = torch.empty((w.m, w.k), dtype=torch.bfloat16, device=DEV)
+
+    def chain():
+        rd_lib.ragged_dot(lhs, up, gs, epilogue=rd_lib.EPI_SILU_GLU, out=h)
+        rd_lib.ragged_dot(h, down, gs, out=o)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        chain()
+    torch.cuda.synchronize()
+    h.fill_(float("nan"))
+    o.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        chain()
+    g.replay()
+    torch.cuda.synchronize()
+    # every row is in a group (the sizes sum to m): nothing may keep the NaN fill
+    assert not bool(torch.isnan(h).any()), "h rows left unwritten"
+    assert not bool(torch.isnan(o).any()), "output rows left unwritten"
+
+    b, _ = oracle.group_bounds(w.group_sizes, w.m)
+    rng = np.random.default_rng(tokens)
+    rows = _sample_rows(b, 0, w.g_total, rng, per_group=4)
+    ridx = torch.from_numpy(rows).to(DEV)
+    cols = _sample_cols(F, rng, 96, tile=128)
+    cidx = torch.from_numpy(cols).to(DEV)
+    ocols = _sample_cols(w.k, rng, 96)
+    ocidx = torch.from_numpy(ocols).to(DEV)
+    a64 = _f64(lhs[ridx])
+    h_rows = h[ridx]
+    h64 = _f64(h_rows)
+    got_h = _f64(h_rows[:, cidx])
+    got_o = _f64(o[ridx][:, ocidx])
+    E = 1e-3 * math.sqrt(w.k) * float(lhs.float().abs().max()) * float(up.float().abs().max())
+    h_amax, d_amax = float(h.float().abs().max()), float(down.float().abs().max())
+    grp = _group_of(rows, b)
+    for j in np.unique(grp):
+        sel = np.nonzero(grp == j)[0]
+        ref, tol = glu_epilogue_tol(a64[sel] @ _f64(up[j][:, cidx]),
+                                    a64[sel] @ _f64(up[j][:, cidx + F]), E)
+        assert_close(got_h[sel], ref, tol, f"ffn {tokens} up group {j}")
+        ref = h64[sel] @ _f64(down[j][:, ocidx])
+        assert_close(got_o[sel], ref, gemm_tol(ref, F, h_amax, d_amax),
+                     f"ffn {tokens} down group {j}")
