@@ -85,7 +85,7 @@ struct alignas(16) GemmShared {
   int32_t total_tiles;
   int32_t zero_lo;  // forward/dx: rows [0, zero_lo) are zero
   int32_t zero_hi;  // forward/dx: rows [zero_hi, L) are zero
-  int32_t epi_tiles;  // tiles whose accumulator the epilogue has taken (paces the zero fill)
+  int32_t fills;      // stages the producer has filled so far (paces the zero fill)
   int32_t bound[kMaxGroups + 1];       // group boundaries, clamped to L
   int32_t tile_start[kMaxGroups + 1];  // first tile of each local group
   uint4 epi[kEpiWarps][32 * 4];        // epilogue staging per warp: 32 rows x 64 bytes
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(ptx::smem_addr(&sh.drain), 1);
     sh.abort_flag = 0;
-    sh.epi_tiles = 0;
+    sh.fills = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0 && args.kc > 0) {
@@ -330,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pend_mask = 0, pend_par = 0;  // fills whose consumption is not yet seen
       uint32_t pend_edge = 0, pend_cpar = 0;  // ... their barrier (edge or not) and its parity
       uint32_t fpar = 0, epar = 0;            // per-slot parities of full / efull
+      int32_t n_fills = 0;
       bool ok = true;
       for (int t = unit; t < total && ok; t += units) {
         const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
@@ -434,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pend_edge = (pend_edge & ~(1u << stage)) | ((edge ? 1u : 0u) << stage);
           pend_cpar = (pend_cpar & ~(1u << stage)) | (cnt_par << stage);
           if (edge) epar ^= 1u << stage; else fpar ^= 1u << stage;
+          *reinterpret_cast<volatile int32_t*>(&sh.fills) = ++n_fills;
           if (++stage == S) {
             stage = 0;
             phase ^= 1;
@@ -579,7 +581,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int piece = lane & 3;    // 16-byte piece of the row's 64 bytes
     int acc = 0;
     uint32_t acc_phase = 0;
-    int tiles_taken = 0;
     for (int t = unit; t < total; t += units) {
       const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
       // first row of this warp's 32 rows and the rows it may write: [lo, hi)
@@ -641,7 +642,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       };
       if (tl.nkb == 0) {
-        if (e == 0 && lane == 0) *reinterpret_cast<volatile int32_t*>(&sh.epi_tiles) = ++tiles_taken;
         const uint32_t z[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
         for (int c = c_begin; c < c_end; ++c) {
           if (F32OUT) {
@@ -660,7 +660,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        tlimit);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
-      if (e == 0 && lane == 0) *reinterpret_cast<volatile int32_t*>(&sh.epi_tiles) = ++tiles_taken;
       ptx::tc_fence_after();
       const uint32_t tbase =
           sh.tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * kBN);
@@ -672,9 +671,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_load_32cols(tbase + kBN / 2 + c * 32, u);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            p[i] = pack_bf16x2(glu_fwd_f32(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
-                               glu_fwd_f32(__uint_as_float(g[2 * i + 1]),
-                                           __uint_as_float(u[2 * i + 1])));
+            p[i] = pack_bf16x2(glu_fwd_fast(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                               glu_fwd_fast(__uint_as_float(g[2 * i + 1]),
+                                            __uint_as_float(u[2 * i + 1])));
           emit(p, col0 + c * 32, 0);
         }
       } else if (EPI == kEpiGluBwd) {
@@ -708,9 +707,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               float dg0, du0, dg1, du1;
-              glu_bwd_f32(bf16_lo(gw[i]), bf16_lo(uw[i]), __uint_as_float(v[w4 * 8 + 2 * i]), dg0, du0);
-              glu_bwd_f32(bf16_hi(gw[i]), bf16_hi(uw[i]), __uint_as_float(v[w4 * 8 + 2 * i + 1]), dg1,
-                          du1);
+              glu_bwd_fast(bf16_lo(gw[i]), bf16_lo(uw[i]), __uint_as_float(v[w4 * 8 + 2 * i]), dg0,
+                           du0);
+              glu_bwd_fast(bf16_hi(gw[i]), bf16_hi(uw[i]), __uint_as_float(v[w4 * 8 + 2 * i + 1]), dg1,
+                           du1);
               pg[w4 * 4 + i] = bf16x2_neg_zero_to_pos(pack_bf16x2(dg0, dg1));
               pu[w4 * 4 + i] = bf16x2_neg_zero_to_pos(pack_bf16x2(du0, du1));
             }
@@ -788,10 +788,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Rows [0, zero_lo) and [zero_hi, L) are two contiguous byte ranges of the
     // output (its rows are contiguous).  Each CTA takes a contiguous 16-byte
     // aligned share of their concatenation and has the bulk-copy engine write it
-    // from a 4 KB zero block in shared memory.  The share goes out in slices,
-    // one more each time the epilogue takes a tile's accumulator, and all of it
-    // before the CTA's last tile: the writes then spread over the run instead
-    // of meeting the first tiles' operand reads in HBM in one burst.
+    // from a 4 KB zero block in shared memory.  The writes are paced by the
+    // CTA's own progress: the bytes issued follow the stages the producer has
+    // filled, reaching the whole share at 4/5 of them, so that they spread over
+    // the run instead of meeting the operand reads in HBM in one burst.
     for (int i = lane; i < 256; i += 32) sh.zeros[i] = make_uint4(0, 0, 0, 0);
     ptx::fence_proxy_async_smem();
     __syncwarp();
@@ -802,39 +802,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t units16 = z_bytes / 16;
       const uint64_t u0 = units16 * blockIdx.x / gridDim.x;
       const uint64_t u1 = units16 * (blockIdx.x + 1) / gridDim.x;
-      const int my_tiles = unit < total ? (total - 1 - unit) / units + 1 : 0;
-      const int slices = my_tiles > 2 ? my_tiles - 1 : 1;
-      const volatile int32_t* taken = &sh.epi_tiles;
-      char* base = reinterpret_cast<char*>(args.out);
-      const uint32_t src = ptx::smem_addr(sh.zeros);
+      if (u1 > u0) {
+        int64_t stages = 0;  // stages this CTA's producer fills in all
+        for (int t = unit; t < total; t += units) stages += decode_tile<OP, PAIR>(sh, args, t).nkb;
+        const uint64_t share = u1 - u0;
+        const volatile int32_t* fills = &sh.fills;
+        char* base = reinterpret_cast<char*>(args.out);
+        const uint32_t src = ptx::smem_addr(sh.zeros);
+        uint64_t done = 0;  // 16-byte units issued
+        uint64_t t_last = ptx::global_timer_ns();
 #pragma unroll 1
-      for (int j = 0; j < slices && u1 > u0; ++j) {
-        if (j > 0 && *taken < j) {
-          // pacing only: give up (and unwind with the CTA) like any other wait
-          const uint64_t t0 = ptx::global_timer_ns();
-          while (*taken < j && !*abort_flag) {
-            if (ptx::global_timer_ns() - t0 > tlimit) {
+        while (done < share) {
+          const int64_t f = *fills;
+          const uint64_t target =
+              (stages == 0 || 5 * f >= 4 * stages)
+                  ? share
+                  : share * static_cast<uint64_t>(5 * f) / static_cast<uint64_t>(4 * stages);
+          if (target <= done) {
+            // pacing only: give up (and unwind with the CTA) like any other wait
+            if (*abort_flag) break;
+            if (ptx::global_timer_ns() - t_last > tlimit) {
               *abort_flag = 1;
               break;
             }
             __nanosleep(500);
+            continue;
           }
-          if (*abort_flag) break;
+          uint64_t b = (u0 + done) * 16;
+          const uint64_t b1 = (u0 + target) * 16;
+          while (b < b1) {
+            const bool low = b < lo_bytes;
+            const uint64_t seg_end = low ? lo_bytes : z_bytes;
+            const uint64_t addr = low ? b : static_cast<uint64_t>(sh.zero_hi) * row_bytes + (b - lo_bytes);
+            uint64_t len = (b1 < seg_end ? b1 : seg_end) - b;
+            if (len > 4096) len = 4096;
+            ptx::bulk_copy_s2g(base + addr, src, static_cast<uint32_t>(len));
+            b += len;
+          }
+          ptx::bulk_commit();
+          done = target;
+          t_last = ptx::global_timer_ns();
         }
-        uint64_t b = (u0 + (u1 - u0) * j / slices) * 16;
-        const uint64_t b1 = (u0 + (u1 - u0) * (j + 1) / slices) * 16;
-        while (b < b1) {
-          const bool low = b < lo_bytes;
-          const uint64_t seg_end = low ? lo_bytes : z_bytes;
-          const uint64_t addr = low ? b : static_cast<uint64_t>(sh.zero_hi) * row_bytes + (b - lo_bytes);
-          uint64_t len = (b1 < seg_end ? b1 : seg_end) - b;
-          if (len > 4096) len = 4096;
-          ptx::bulk_copy_s2g(base + addr, src, static_cast<uint32_t>(len));
-          b += len;
-        }
-        ptx::bulk_commit();
+        ptx::bulk_wait_read_all();
       }
-      ptx::bulk_wait_read_all();
     }
   }
 

@@ -36,6 +36,58 @@ __device__ __forceinline__ void glu_bwd_f32(float g, float u, float d, float& d_
   d_gate = __fmul_rn(__fmul_rn(d, u), dsil);
 }
 
+// ---------------------------------------------------------------------------
+// The fused epilogues (GLU forward after the up projection, GLU backward after
+// dx of the down projection) are compared with the float64 values within a
+// bf16 ulp, not bit for bit, and there the GLU costs more issue slots than the
+// rest of the epilogue.  They evaluate the logistic in its two-sided stable
+// form: t = exp(-|g|) lies in (0, 1], r = 1 / (1 + t) in [1/2, 1), and
+//   g >= 0: sig = r,     1 - sig = t r
+//   g <  0: sig = t r,   1 - sig = r,
+// so the reciprocal never sees a denominator above 2 and 1 - sig never
+// cancels.  exp comes from the hardware base-2 exponential,
+// exp(x) = 2^(x log2 e), and 1/x from the hardware reciprocal; both are the
+// .approx forms without flush-to-zero, so t keeps its subnormal values down
+// to 2^-149: gates between -103 and -88.7, where exp(-g) overflows in the op
+// sequence above and silu comes out zero, keep their tiny silu.  Relative error of
+// sig, silu and their products: a few f32 ulps.  +-inf, NaN and -0 gates give
+// the results of the op sequence above.
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// sig = logistic(g) and 1 - sig
+__device__ __forceinline__ void sigmoid_two_sided(float g, float& sig, float& one_minus_sig) {
+  const float t = exp2_approx(-fabsf(g) * 1.44269504088896341f);  // exp(-|g|)
+  const float r = rcp_approx(1.0f + t);
+  const float tr = t * r;
+  const bool pos = g >= 0.0f;
+  sig = pos ? r : tr;
+  one_minus_sig = pos ? tr : r;
+}
+
+__device__ __forceinline__ float glu_fwd_fast(float g, float u) {
+  float sig, om;
+  sigmoid_two_sided(g, sig, om);
+  return (g * sig) * u;
+}
+
+__device__ __forceinline__ void glu_bwd_fast(float g, float u, float d, float& d_gate,
+                                             float& d_up) {
+  float sig, om;
+  sigmoid_two_sided(g, sig, om);
+  d_up = d * (g * sig);
+  d_gate = (d * u) * (sig * (1.0f + g * om));
+}
+
 // two floats -> packed bf16x2 (round to nearest even), lower half first
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

@@ -272,6 +272,72 @@ def test_dx_glu_bwd(rd_lib, m, f, n, off, gl, limit):
     run_dx_glu_bwd(rd_lib, m, f, n, sizes, off=off, gl=gl, limit=limit, seed=f + n + off)
 
 
+# Gates at and past the ends of binary32's exp range (exp(-g) overflows below
+# -88.72 and exp(-|g|) goes subnormal below -87.34 and to zero below -103.28),
+# large magnitudes and the special values.  The GEMM in front of the GLU is
+# made exact (one-hot rows against the chosen values) so the epilogue alone is
+# measured: within 1 bf16 ulp of float64, NaN for NaN, equal infinities.
+SPECIAL_GATES = [float("-inf"), float("inf"), float("nan"), -0.0, 0.0, -1e4, -110.0, -103.0,
+                 -100.0, -95.0, -91.0, -89.0, -88.5, -88.0, -87.5, -87.0, -60.0, -20.0, -5.0,
+                 -1.0, -1e-30, 1e-30, 0.5, 1.0, 5.0, 20.0, 60.0, 88.0, 89.0, 100.0, 1e4, 1e30]
+SPECIAL_UPS = [0.5, -1.25, 1.0, -0.0, 0.75, -0.5, 0.0, 1.0]
+
+
+def _special_table(rows, cols, seed):
+    """rows x cols bf16 gates / ups: every special gate in every row, shuffled per row."""
+    rng = np.random.default_rng(seed)
+    g = np.array([rng.permutation(np.resize(SPECIAL_GATES, cols)) for _ in range(rows)], np.float32)
+    u = np.array([rng.permutation(np.resize(SPECIAL_UPS, cols)) for _ in range(rows)], np.float32)
+    return torch.from_numpy(g).to(torch.bfloat16), torch.from_numpy(u).to(torch.bfloat16)
+
+
+def test_fused_glu_forward_special_gates(rd_lib):
+    """The fused forward GLU on gates across exp's range edges and special values.
+
+    Group j's weight block holds table row j in its row 0 and zeros elsewhere,
+    and every lhs row is the unit vector e_0, so each accumulator is exactly one
+    table value (no 0 * inf products).
+    """
+    k, F, groups, per = 16, 64, 16, 6
+    m = groups * per
+    g, u = _special_table(groups, F, 11)
+    rhs = torch.zeros((groups, k, 2 * F), dtype=torch.bfloat16)
+    rhs[:, 0, :F] = g
+    rhs[:, 0, F:] = u
+    lhs = torch.zeros((m, k), dtype=torch.bfloat16)
+    lhs[:, 0] = 1.0
+    out = torch.empty((m, F), dtype=torch.bfloat16, device=DEV)
+    rd_lib.ragged_dot(lhs.to(DEV), rhs.to(DEV), _i32([per] * groups), epilogue=rd_lib.EPI_SILU_GLU,
+                      out=out)
+    torch.cuda.synchronize()
+    from oracle import glu as oglu
+    sel = np.arange(m) // per
+    ref = oglu.glu_fwd_f64(_f64(g)[sel], _f64(u)[sel])
+    assert_close(_f64(out.cpu()), ref, obf.ulp(ref), "fused GLU forward, special gates")
+
+
+def test_fused_glu_backward_special_gates(rd_lib):
+    """The fused GLU backward (dx of the down projection) on the same gates."""
+    n, f, m = 16, 64, 96
+    g, u = _special_table(m, f, 12)
+    fused = torch.cat([g, u], dim=1)
+    rng = np.random.default_rng(13)
+    dvals = torch.from_numpy(rng.choice([1.5, -0.75, 2.0, -0.5], size=(f, n)).astype(np.float32))
+    w = dvals.to(torch.bfloat16).reshape(1, f, n)           # dh[i, c] = w[c, i % n]
+    d_out = torch.zeros((m, n), dtype=torch.bfloat16)
+    d_out[torch.arange(m), torch.arange(m) % n] = 1.0
+    out = torch.empty((m, 2 * f), dtype=torch.bfloat16, device=DEV)
+    rd_lib.ragged_dot_trans_rhs_glu_bwd(d_out.to(DEV), w.to(DEV), fused.to(DEV), _i32([m]), out=out)
+    torch.cuda.synchronize()
+    bits = obf.torch_bf16_bits(out)
+    assert not np.any(bits == 0x8000), "a -0 survived the -0 -> +0 fix"
+    from oracle import glu as oglu
+    dh = _f64(w[0]).T[np.arange(m) % n]                     # [m, f]
+    dg, du = oglu.glu_bwd_f64(_f64(g), _f64(u), dh)
+    ref = np.concatenate([dg, du], axis=1)
+    assert_close(_f64(out.cpu()), ref, obf.ulp(ref), "fused GLU backward, special gates")
+
+
 # ------------------------------------------------------------------ dw
 DW_SIZES = [0, 1, 63, 64, 65, 200, 0, 130]   # sum 523
 
