@@ -5,7 +5,8 @@
 // commit message, kernels/ragged/glu_rows.py): silu(gate) * up over rows
 // [0, limit) only, gate and up read in place from the fused buffer; the
 // backward recomputes the forward and writes [d_gate | d_up] in one pass with
-// the -0 -> +0 fix.  The arithmetic is in glu_math.cuh.
+// the -0 -> +0 fix.  The arithmetic is in glu_math.cuh (the two-sided
+// logistic with the op sequence's results wherever those are special).
 //
 // Both kernels are HBM-bound streams: one warp per row, 16-byte vector loads
 // that bypass L1, several vectors per lane in flight before the math.
@@ -34,14 +35,14 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {
 }
 
 __device__ __forceinline__ uint32_t glu2(uint32_t g, uint32_t u) {
-  return pack_bf16x2(glu_fwd_f32(bf16_lo(g), bf16_lo(u)), glu_fwd_f32(bf16_hi(g), bf16_hi(u)));
+  return pack_bf16x2(glu_fwd_seq(bf16_lo(g), bf16_lo(u)), glu_fwd_seq(bf16_hi(g), bf16_hi(u)));
 }
 
 __device__ __forceinline__ void glu_bwd2(uint32_t g, uint32_t u, uint32_t d, uint32_t& dg,
                                          uint32_t& du) {
   float g0, u0, g1, u1;
-  glu_bwd_f32(bf16_lo(g), bf16_lo(u), bf16_lo(d), g0, u0);
-  glu_bwd_f32(bf16_hi(g), bf16_hi(u), bf16_hi(d), g1, u1);
+  glu_bwd_seq(bf16_lo(g), bf16_lo(u), bf16_lo(d), g0, u0);
+  glu_bwd_seq(bf16_hi(g), bf16_hi(u), bf16_hi(d), g1, u1);
   dg = bf16x2_neg_zero_to_pos(pack_bf16x2(g0, g1));
   du = bf16x2_neg_zero_to_pos(pack_bf16x2(u0, u1));
 }
