@@ -588,6 +588,34 @@ def run_rd(args):
     e2e_value = world * flops / (e2e_ms / e2e_steps * 1e-3) / 1e12
     h2d = h_lhs.numel() * 2 + h_rhs.numel() * 2 + h_gs.numel() * 4
     d2h = h_out[0].numel() * 2
+
+    # What bounds the end-to-end step: the host link.  The step's own upload and
+    # download run concurrently on the two copy streams (as in the pipeline),
+    # each timed on its stream; the step can be no faster than the slower
+    # direction or the forward itself.
+    def link_gbs(reps=3):
+        d_lhs, d_rhs, d_gs, d_out = bufs[0]
+        ti = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        to = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        torch.cuda.synchronize()
+        ti[0].record(s_in)
+        to[0].record(s_out)
+        for _ in range(reps):
+            with torch.cuda.stream(s_in):
+                d_lhs.copy_(h_lhs, non_blocking=True)
+                d_rhs.copy_(h_rhs, non_blocking=True)
+                d_gs.copy_(h_gs, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                h_out[0].copy_(d_out, non_blocking=True)
+        ti[1].record(s_in)
+        to[1].record(s_out)
+        torch.cuda.synchronize()
+        return (reps * h2d / (ti[0].elapsed_time(ti[1]) * 1e-3) / 1e9,
+                reps * d2h / (to[0].elapsed_time(to[1]) * 1e-3) / 1e9)
+
+    h2d_gbs, d2h_gbs = link_gbs()
+    step_floor_s = max(h2d / (h2d_gbs * 1e9), d2h / (d2h_gbs * 1e9), ms_per_step * 1e-3)
+    e2e_limit = world * flops / step_floor_s / 1e12
     del bufs
     torch.cuda.empty_cache()
 
@@ -626,7 +654,10 @@ def run_rd(args):
                          "kernel": "grouped_gemm_kernel<fwd>"},
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "pipelined": "upload i+1 / forward i / download i-1 on three streams"},
+                    "pipelined": "upload i+1 / forward i / download i-1 on three streams",
+                    "bound": {"h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
+                              "measured": "step's upload and download, concurrent",
+                              "limit": e2e_limit, "frac": e2e_value / e2e_limit}},
             "gpu_launches": args.steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
