@@ -129,7 +129,10 @@ rd_status rd_ragged_dot_trans_rhs(const void* lhs, const void* rhs, void* out, i
  * #5760 (commit message: the GLU backward writes [d_gate | d_up] in one pass,
  * recomputing the forward from the saved fused buffer).  Unlike running
  * rd_ragged_dot_trans_rhs then rd_glu_bwd, dh is used unrounded and never
- * goes to memory.
+ * goes to memory.  Accuracy: within one bf16 ulp of the exact value of the
+ * formulas, plus the GEMM error of dh carried through them; the logistic is
+ * evaluated as 1 / (1 + exp(-|g|)) on either side of 0, so gates far below
+ * zero keep their tiny gradients.
  *
  *   d_out [m, n] bf16, rhs [g_local, f, n] bf16 (the down weights, forward
  *   h [m, f] @ rhs[j] [f, n]), fused [m, 2f] bf16, d_fused [m, 2f] bf16.
@@ -186,6 +189,9 @@ rd_status rd_trans_ragged_dot_f32(const void* x, const void* y, float* out, int6
  * Defined by MaxText PR #5760 (commit message, kernels/ragged/glu_rows.py:
  * gate and up read in place from the fused buffer, XLA's op sequence
  * negate, exp, +1, divide, multiply in f32, rounded only at the output).
+ * Accuracy: within one bf16 ulp of the exact value; where that op sequence
+ * gives an infinity, a NaN or (for g below -88.72, where exp(-g) overflows
+ * binary32) a signed zero, the output has exactly its bits.
  *
  *   fused [rows, 2f] bf16, out [rows, f] bf16, limit device int32 or NULL.
  * Requires f % 8 == 0, 16-byte aligned pointers, out not overlapping fused.
@@ -202,7 +208,9 @@ rd_status rd_glu_fwd(const void* fused, void* out, int64_t rows, int64_t f,
  *   and any result that rounds to -0 is stored as +0; rows r < L only.
  * Defined by MaxText PR #5760 (commit message: the backward writes
  * [d_gate | d_up] in one pass with the -0 -> +0 fix, recomputing the
- * forward from the saved fused buffer).
+ * forward from the saved fused buffer).  Accuracy as rd_glu_fwd: within one
+ * bf16 ulp of the exact value, and the op sequence's bits wherever it gives
+ * an infinity, a NaN or a zero from the overflow of exp(-g).
  *
  *   fused [rows, 2f] bf16, d_out [rows, f] bf16, d_fused [rows, 2f] bf16.
  * Requires f % 8 == 0, 16-byte aligned pointers, d_fused not overlapping
