@@ -247,14 +247,19 @@ def run_ops(rd, device, stream, peaks):
     import numpy as np
     import torch
 
-    from workloads import backward_pair, decode_fwd, normal_bf16, packed_glu_fwd
+    from workloads import backward_pair, decode_fwd, normal_bf16, packed_glu_fwd, tiny_fwd
 
     P = peaks["bf16_tflops"] * 1e12
     BW = peaks["hbm_gbs"] * 1e9
     res = {}
 
-    def med(fn, steps=20, warmup=3):
+    spread = []  # (entry, key prefix, p10 us, p90 us) of each timed call
+
+    def med(fn, steps=20, warmup=3, entry=None, prefix=""):
         per, _ = time_launches(fn, steps, warmup, stream)
+        if entry is not None:
+            q = statistics.quantiles(per, n=10)
+            spread.append((entry, prefix, q[0] * 1e3, q[-1] * 1e3))
         return statistics.median(per) * 1e-3
 
     with torch.cuda.stream(stream):
@@ -270,18 +275,19 @@ def run_ops(rd, device, stream, peaks):
         F = 2.0 * rows * w.k * w.n
         zero_rows = w.limit - rows
         B = rows * w.k * 2 + w.g_local * w.k * w.n * 2 + w.limit * (w.n // 2) * 2 + 4 * w.g_total
-        t = med(lambda: rd.ragged_dot(lhs, rhs, gs, w.group_offset, lim, rd.EPI_SILU_GLU, out))
+        t = med(lambda: rd.ragged_dot(lhs, rhs, gs, w.group_offset, lim, rd.EPI_SILU_GLU, out),
+                entry="packed_glu_fwd")
         res["packed_glu_fwd"] = {"us": t * 1e6, "tflops": F / t / 1e12, "gbs": B / t / 1e9,
                                  "bound": "tensor", "frac": max(F / P, B / BW) / t,
                                  "local_rows": rows, "zero_rows": zero_rows}
         # standalone GLU on the same packed buffer shape
         fused = normal_bf16((w.m, 2 * 1024), 1.0, 32, device)
         gout = torch.empty((w.m, 1024), dtype=torch.bfloat16, device=device)
-        t = med(lambda: rd.glu_fwd(fused, lim, gout))
+        t = med(lambda: rd.glu_fwd(fused, lim, gout), entry="glu_fwd")
         Bg = w.limit * 1024 * 2 * 3
         res["glu_fwd"] = {"us": t * 1e6, "gbs": Bg / t / 1e9, "bound": "hbm", "frac": Bg / BW / t}
         dfused = torch.empty_like(fused)
-        t = med(lambda: rd.glu_bwd(fused, gout, lim, dfused))
+        t = med(lambda: rd.glu_bwd(fused, gout, lim, dfused), entry="glu_bwd")
         Bb = w.limit * 1024 * 2 * 5
         res["glu_bwd"] = {"us": t * 1e6, "gbs": Bb / t / 1e9, "bound": "hbm", "frac": Bb / BW / t}
         del lhs, rhs, out, fused, gout, dfused
@@ -295,13 +301,13 @@ def run_ops(rd, device, stream, peaks):
         dfused2 = torch.empty_like(fused2)
         dh = torch.empty((w.m, 1024), dtype=torch.bfloat16, device=device)
         t_fused = med(lambda: rd.ragged_dot_trans_rhs_glu_bwd(d_out, w_down, fused2, gs, w.group_offset,
-                                                              lim, dfused2))
+                                                              lim, dfused2), entry="packed_dx_glu_bwd")
 
         def unfused():
             rd.ragged_dot_trans_rhs(d_out, w_down, gs, w.group_offset, lim, dh)
             rd.glu_bwd(fused2, dh, lim, dfused2)
 
-        t_unfused = med(unfused)
+        t_unfused = med(unfused, entry="packed_dx_glu_bwd", prefix="unfused_")
         F2 = 2.0 * rows * 1024 * 4096
         B2 = (rows * 4096 * 2 + w.g_local * 1024 * 4096 * 2 + rows * 2048 * 2
               + w.limit * 2048 * 2 + 4 * w.g_total)
@@ -317,7 +323,7 @@ def run_ops(rd, device, stream, peaks):
         wt = torch.rand((w.m,), device=device)
         grad = torch.empty_like(g)
         dot = torch.empty((w.m,), dtype=torch.float32, device=device)
-        t = med(lambda: rd.unsort_bwd_rows(g, y, wt, lim, grad, dot))
+        t = med(lambda: rd.unsort_bwd_rows(g, y, wt, lim, grad, dot), entry="unsort_bwd_rows")
         Bu = w.limit * 4096 * 2 * 3 + w.limit * 8
         res["unsort_bwd_rows"] = {"us": t * 1e6, "gbs": Bu / t / 1e9, "bound": "hbm",
                                   "frac": Bu / BW / t}
@@ -334,11 +340,11 @@ def run_ops(rd, device, stream, peaks):
         dw = torch.empty((w.g_total, w.k, w.n), dtype=torch.bfloat16, device=device)
         F = 2.0 * w.m * w.k * w.n
         live = int((w.group_sizes > 0).sum())
-        t = med(lambda: rd.ragged_dot_trans_rhs(do, wt, gs, out=dx))
+        t = med(lambda: rd.ragged_dot_trans_rhs(do, wt, gs, out=dx), entry="dx")
         B = w.m * w.n * 2 + live * w.k * w.n * 2 + w.m * w.k * 2
         res["dx"] = {"us": t * 1e6, "tflops": F / t / 1e12, "bound": "tensor",
                      "frac": max(F / P, B / BW) / t}
-        t = med(lambda: rd.trans_ragged_dot(x, do, gs, out=dw))
+        t = med(lambda: rd.trans_ragged_dot(x, do, gs, out=dw), entry="dw")
         B = w.m * w.k * 2 + w.m * w.n * 2 + w.g_total * w.k * w.n * 2
         res["dw"] = {"us": t * 1e6, "tflops": F / t / 1e12, "bound": "tensor",
                      "frac": max(F / P, B / BW) / t}
@@ -364,22 +370,37 @@ def run_ops(rd, device, stream, peaks):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 pair()
-            t_pair = med(g.replay, steps=50, warmup=5)
-            t_up = med(lambda: rd.ragged_dot(lhs, up, gs, epilogue=rd.EPI_SILU_GLU, out=h), 50, 5)
-            t_down = med(lambda: rd.ragged_dot(h, down, gs, out=o), 50, 5)
+            tag = "decode_skewed" if skew else "decode_uniform"
+            t_pair = med(g.replay, steps=50, warmup=5, entry=tag, prefix="graph_pair_")
+            t_up = med(lambda: rd.ragged_dot(lhs, up, gs, epilogue=rd.EPI_SILU_GLU, out=h), 50, 5,
+                       entry=tag, prefix="up_")
+            t_down = med(lambda: rd.ragged_dot(h, down, gs, out=o), 50, 5, entry=tag, prefix="down_")
             live = int((w.group_sizes > 0).sum())
             B_up = w.m * w.k * 2 + live * w.k * w.n * 2 + w.m * (w.n // 2) * 2
             B_dn = w.m * (w.n // 2) * 2 + live * (w.n // 2) * w.k * 2 + w.m * w.k * 2
-            tag = "decode_skewed" if skew else "decode_uniform"
             res[tag] = {"graph_pair_us": t_pair * 1e6, "up_us": t_up * 1e6, "down_us": t_down * 1e6,
                         "bound": "hbm", "live_groups": live,
                         "up_frac": B_up / BW / t_up, "down_frac": B_dn / BW / t_down,
                         "pair_frac": (B_up + B_dn) / BW / t_pair}
             del lhs, up, down, h, o, g
             torch.cuda.empty_cache()
+        # the tiny workload (L2-resident, launch-latency bound): time per call
+        w = tiny_fwd()
+        lhs = normal_bf16((w.m, w.k), w.lhs_var, 60, device)
+        rhs = normal_bf16((w.g_total, w.k, w.n), w.rhs_var, 61, device)
+        gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=device)
+        out = torch.empty((w.m, w.n), dtype=torch.bfloat16, device=device)
+        t = med(lambda: rd.ragged_dot(lhs, rhs, gs, out=out), steps=100, warmup=10, entry="tiny")
+        res["tiny"] = {"us": t * 1e6, "bound": "latency", "workload": w.name,
+                       "note": "L2-resident; device time between events around one launch"}
+        del lhs, rhs, out
         # the expert FFN forward (up with GLU, then down) as one CUDA graph, from decode
         # to prefill batch sizes: where the weight stream stops bounding the time
         res["ffn_sweep"] = ffn_sweep(rd, device, stream, peaks)
+    for entry, prefix, p10, p90 in spread:
+        if entry in res:
+            res[entry][prefix + "p10_us"] = p10
+            res[entry][prefix + "p90_us"] = p90
     return res
 
 
@@ -489,6 +510,7 @@ def run_reference(args):
         "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "sample": desc},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "host_cores": os.cpu_count(),
                          "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -627,7 +649,7 @@ def run_rd(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, dt, desc, _ = oracle_sample_run(w, h_lhs, h_rhs, target_s=10.0)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": desc, "seconds": round(dt, 2)}
+               "host_cores": os.cpu_count(), "sample": desc, "seconds": round(dt, 2)}
 
     if rank == 0:
         line = {
@@ -659,6 +681,9 @@ def run_rd(args):
                               "measured": "step's upload and download, concurrent",
                               "limit": e2e_limit, "frac": e2e_value / e2e_limit}},
             "gpu_launches": args.steps,
+            "launch_ms": {"median": statistics.median(per),
+                          "p10": statistics.quantiles(per, n=10)[0] if len(per) > 1 else per[0],
+                          "p90": statistics.quantiles(per, n=10)[-1] if len(per) > 1 else per[0]},
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
             "ops": ops,
