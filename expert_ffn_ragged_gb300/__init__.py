@@ -107,14 +107,34 @@ def _bf16_2d(t, name):
         raise ValueError(f"{name} must be a contiguous 2-D bf16 CUDA tensor")
 
 
+def _bf16_3d(t, name, what):
+    import torch
+
+    if t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {what} bf16 CUDA tensor")
+
+
+def _out(t, shape, dtype, name="out"):
+    """A caller-supplied output must match exactly: the library only sees its pointer."""
+    if (tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_cuda
+            or not t.is_contiguous()):
+        raise ValueError(f"{name} must be a contiguous {list(shape)} {dtype} CUDA tensor")
+
+
+def _scalar_i32(t, name):
+    import torch
+
+    if t is not None and (t.dtype != torch.int32 or t.numel() != 1 or not t.is_cuda):
+        raise ValueError(f"{name} must be a one-element int32 CUDA tensor")
+
+
 def _group_args(group_sizes, limit, status):
     import torch
 
     if group_sizes.dtype != torch.int32 or group_sizes.dim() != 1 or not group_sizes.is_cuda:
         raise ValueError("group_sizes must be a 1-D int32 CUDA tensor")
-    for name, t in (("limit", limit), ("status", status)):
-        if t is not None and (t.dtype != torch.int32 or t.numel() != 1 or not t.is_cuda):
-            raise ValueError(f"{name} must be a one-element int32 CUDA tensor")
+    _scalar_i32(limit, "limit")
+    _scalar_i32(status, "status")
 
 
 def ragged_dot(lhs, rhs, group_sizes, group_offset: int = 0, limit=None, epilogue: int = EPI_NONE,
@@ -125,8 +145,7 @@ def ragged_dot(lhs, rhs, group_sizes, group_offset: int = 0, limit=None, epilogu
     lib = load()
     _bf16_2d(lhs, "lhs")
     _group_args(group_sizes, limit, status)
-    if rhs.dtype != torch.bfloat16 or rhs.dim() != 3 or not rhs.is_contiguous():
-        raise ValueError("rhs must be a contiguous [g_local, k, n] bf16 CUDA tensor")
+    _bf16_3d(rhs, "rhs", "[g_local, k, n]")
     m, k = lhs.shape
     g_local, k2, n = rhs.shape
     if k2 != k:
@@ -134,6 +153,7 @@ def ragged_dot(lhs, rhs, group_sizes, group_offset: int = 0, limit=None, epilogu
     n_out = n // 2 if epilogue == EPI_SILU_GLU else n
     if out is None:
         out = torch.empty((m, n_out), dtype=torch.bfloat16, device=lhs.device)
+    _out(out, (m, n_out), torch.bfloat16)
     code = lib.rd_ragged_dot(_ptr(lhs), _ptr(rhs), _ptr(out), m, k, n, _ptr(group_sizes),
                              group_sizes.numel(), group_offset, g_local, _ptr(limit),
                              int(epilogue), _ptr(status), _stream(stream))
@@ -149,14 +169,14 @@ def ragged_dot_trans_rhs(lhs, rhs, group_sizes, group_offset: int = 0, limit=Non
     lib = load()
     _bf16_2d(lhs, "lhs")
     _group_args(group_sizes, limit, status)
-    if rhs.dtype != torch.bfloat16 or rhs.dim() != 3 or not rhs.is_contiguous():
-        raise ValueError("rhs must be a contiguous [g_local, k, n] bf16 CUDA tensor")
+    _bf16_3d(rhs, "rhs", "[g_local, k, n]")
     m, n = lhs.shape
     g_local, k, n2 = rhs.shape
     if n2 != n:
         raise ValueError("lhs and rhs disagree on n")
     if out is None:
         out = torch.empty((m, k), dtype=torch.bfloat16, device=lhs.device)
+    _out(out, (m, k), torch.bfloat16)
     code = lib.rd_ragged_dot_trans_rhs(_ptr(lhs), _ptr(rhs), _ptr(out), m, k, n, _ptr(group_sizes),
                                        group_sizes.numel(), group_offset, g_local, _ptr(limit),
                                        _ptr(status), _stream(stream))
@@ -176,14 +196,14 @@ def ragged_dot_trans_rhs_glu_bwd(d_out, rhs, fused, group_sizes, group_offset: i
     _bf16_2d(d_out, "d_out")
     _bf16_2d(fused, "fused")
     _group_args(group_sizes, limit, status)
-    if rhs.dtype != torch.bfloat16 or rhs.dim() != 3 or not rhs.is_contiguous():
-        raise ValueError("rhs must be a contiguous [g_local, f, n] bf16 CUDA tensor")
+    _bf16_3d(rhs, "rhs", "[g_local, f, n]")
     m, n = d_out.shape
     g_local, f, n2 = rhs.shape
     if n2 != n or fused.shape != (m, 2 * f):
         raise ValueError("shapes disagree: d_out [m, n], rhs [g, f, n], fused [m, 2f]")
     if out is None:
         out = torch.empty((m, 2 * f), dtype=torch.bfloat16, device=d_out.device)
+    _out(out, (m, 2 * f), torch.bfloat16)
     code = lib.rd_ragged_dot_trans_rhs_glu_bwd(
         _ptr(d_out), _ptr(rhs), _ptr(fused), _ptr(out), m, f, n, _ptr(group_sizes),
         group_sizes.numel(), group_offset, g_local, _ptr(limit), _ptr(status), _stream(stream))
@@ -208,6 +228,7 @@ def trans_ragged_dot(x, y, group_sizes, group_offset: int = 0, g_local: Optional
         g_local = group_sizes.numel() - group_offset
     if out is None:
         out = torch.empty((g_local, k, n), dtype=torch.bfloat16, device=x.device)
+    _out(out, (g_local, k, n), torch.bfloat16)
     code = lib.rd_trans_ragged_dot(_ptr(x), _ptr(y), _ptr(out), m, k, n, _ptr(group_sizes),
                                    group_sizes.numel(), group_offset, g_local, _ptr(limit),
                                    _ptr(status), _stream(stream))
@@ -234,8 +255,7 @@ def trans_ragged_dot_f32(x, y, group_sizes, group_offset: int = 0, g_local: Opti
         if accumulate:
             raise ValueError("accumulate needs an existing out buffer")
         out = torch.empty((g_local, k, n), dtype=torch.float32, device=x.device)
-    if out.dtype != torch.float32 or out.shape != (g_local, k, n) or not out.is_contiguous():
-        raise ValueError("out must be a contiguous [g_local, k, n] float32 CUDA tensor")
+    _out(out, (g_local, k, n), torch.float32)
     code = lib.rd_trans_ragged_dot_f32(_ptr(x), _ptr(y), _ptr(out), m, k, n, _ptr(group_sizes),
                                        group_sizes.numel(), group_offset, g_local, _ptr(limit),
                                        1 if accumulate else 0, _ptr(status), _stream(stream))
@@ -249,10 +269,12 @@ def glu_fwd(fused, limit=None, out=None, stream=None):
 
     lib = load()
     _bf16_2d(fused, "fused")
+    _scalar_i32(limit, "limit")
     rows, w = fused.shape
     f = w // 2
     if out is None:
         out = torch.empty((rows, f), dtype=torch.bfloat16, device=fused.device)
+    _out(out, (rows, f), torch.bfloat16)
     code = lib.rd_glu_fwd(_ptr(fused), _ptr(out), rows, f, _ptr(limit), _stream(stream))
     _check(code, "rd_glu_fwd")
     return out
@@ -269,8 +291,10 @@ def glu_bwd(fused, d_out, limit=None, out=None, stream=None):
     f = w // 2
     if d_out.shape != (rows, f):
         raise ValueError("d_out must be [rows, f]")
+    _scalar_i32(limit, "limit")
     if out is None:
         out = torch.empty((rows, 2 * f), dtype=torch.bfloat16, device=fused.device)
+    _out(out, (rows, 2 * f), torch.bfloat16)
     code = lib.rd_glu_bwd(_ptr(fused), _ptr(d_out), _ptr(out), rows, f, _ptr(limit),
                           _stream(stream))
     _check(code, "rd_glu_bwd")
@@ -289,10 +313,13 @@ def unsort_bwd_rows(g, y, w, limit=None, grad=None, dot=None, stream=None):
         raise ValueError("g and y must have the same shape")
     if w.dtype != torch.float32 or w.shape != (rows,) or not w.is_cuda:
         raise ValueError("w must be a [rows] float32 CUDA tensor")
+    _scalar_i32(limit, "limit")
     if grad is None:
         grad = torch.empty_like(g)
     if dot is None:
         dot = torch.empty((rows,), dtype=torch.float32, device=g.device)
+    _out(grad, (rows, hidden), torch.bfloat16, "grad")
+    _out(dot, (rows,), torch.float32, "dot")
     code = lib.rd_unsort_bwd_rows(_ptr(g), _ptr(y), _ptr(w), _ptr(grad), _ptr(dot), rows, hidden,
                                   _ptr(limit), _stream(stream))
     _check(code, "rd_unsort_bwd_rows")

@@ -532,3 +532,31 @@ def test_limit_zero_writes_nothing_anywhere(rd_lib):
     torch.cuda.synchronize()
     for o in outs:
         assert bool((o.view(torch.int16) == SENT).all())
+
+
+def test_binding_rejects_mismatched_buffers(rd_lib):
+    """The C ABI sees only pointers and sizes, so the binding checks caller-supplied outputs."""
+    lhs = torch.zeros((64, 32), dtype=torch.bfloat16, device=DEV)
+    rhs = torch.zeros((2, 32, 64), dtype=torch.bfloat16, device=DEV)
+    gs = _i32([32, 32])
+    bad = [
+        lambda: rd_lib.ragged_dot(lhs, rhs, gs, out=torch.empty((63, 64), dtype=torch.bfloat16, device=DEV)),
+        lambda: rd_lib.ragged_dot(lhs, rhs, gs, epilogue=rd_lib.EPI_SILU_GLU,
+                                  out=torch.empty((64, 64), dtype=torch.bfloat16, device=DEV)),
+        lambda: rd_lib.ragged_dot(lhs, rhs, gs, out=torch.empty((64, 64), dtype=torch.float32, device=DEV)),
+        lambda: rd_lib.ragged_dot(lhs, rhs, gs, out=torch.empty((64, 128), dtype=torch.bfloat16,
+                                                                 device=DEV)[:, ::2]),
+        lambda: rd_lib.ragged_dot(lhs, rhs.cpu(), gs),
+        lambda: rd_lib.ragged_dot_trans_rhs(lhs[:, :32], rhs.transpose(1, 2).contiguous(), gs,
+                                            out=torch.empty((64, 63), dtype=torch.bfloat16, device=DEV)),
+        lambda: rd_lib.trans_ragged_dot(lhs, lhs, gs, out=torch.empty((2, 32, 31), dtype=torch.bfloat16,
+                                                                        device=DEV)),
+        lambda: rd_lib.glu_fwd(lhs, out=torch.empty((64, 32), dtype=torch.bfloat16, device=DEV)),
+        lambda: rd_lib.glu_fwd(lhs, limit=_i32([1, 2])),
+    ]
+    for i, call in enumerate(bad):
+        try:
+            call()
+        except ValueError:
+            continue
+        raise AssertionError(f"case {i} was accepted")
