@@ -520,16 +520,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             const uint32_t a_addr = ptx::smem_addr(a_st);
             const uint32_t b_addr = ptx::smem_addr(b_st);
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              if (kk < kk0) continue;
+            // one 16-deep K step of the block into the accumulator
+            auto mma_step = [&](int kk, uint32_t accum) {
               const uint64_t adesc = a_mn ? ptx::sw128_desc(a_addr + kk * 2048, kBK * 128, 1024)
                                           : ptx::sw128_desc(a_addr + kk * 32, 16, 1024);
               const uint64_t bdesc = b_mn ? ptx::sw128_desc(b_addr + kk * 2048, b_lbo, 1024)
                                           : ptx::sw128_desc(b_addr + kk * 32, 16, 1024);
-              const uint32_t accum = (kb > 0 || kk > kk0) ? 1u : 0u;
               if (PAIR) ptx::tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, accum);
               else ptx::tc_mma_bf16(d_tmem, adesc, bdesc, idesc, accum);
+            };
+            if (kk0 == 0) {
+              // every block but a dw group's straddling last one: four MMAs back to
+              // back (with a skip test in front of each, dw's issue took ~1.3x as long)
+#pragma unroll
+              for (int kk = 0; kk < kBK / 16; ++kk) mma_step(kk, (kb > 0 || kk > 0) ? 1u : 0u);
+            } else {
+#pragma unroll 1
+              for (int kk = kk0; kk < kBK / 16; ++kk) mma_step(kk, (kb > 0 || kk > kk0) ? 1u : 0u);
             }
             if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&sh.empty[stage]), 0x3);
             else ptx::tc_commit(ptx::smem_addr(&sh.empty[stage]));
