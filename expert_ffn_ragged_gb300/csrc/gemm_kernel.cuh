@@ -469,13 +469,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (!PAIR || rank == 0) {
+    // One thread does all of it: waits, issue and commits.  (Waiting with the
+    // whole warp and voting on the result cost ~100 ns per K block, during which
+    // the tensor pipe ran dry.)
+    if ((!PAIR || rank == 0) && lane == 0) {
       constexpr bool a_mn = (OP == kOpDw);
       constexpr bool b_mn = (OP != kOpDx);
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(TM, kBN, a_mn, b_mn);
       constexpr uint32_t b_lbo = kBK * 128;  // MN-major B: stride between 64-wide chunks
       int stage = 0;
-      uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       uint32_t pready_par = 0;  // per-slot parity of pready (edge blocks)
@@ -484,9 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = unit; t < total && ok; t += units) {
         const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
         if (tl.nkb == 0) continue;
-        ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.tempty[acc]), acc_phase ^ 1,
-                                            abort_flag, tlimit);
-        ok = __all_sync(0xFFFFFFFFu, ok);
+        ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.tempty[acc]), acc_phase ^ 1, abort_flag,
+                                    tlimit);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = sh.tmem_base + static_cast<uint32_t>(acc * kBN);
@@ -512,61 +513,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         abort_flag, tlimit);
             full_par ^= 1u << stage;
           }
-          ok = __all_sync(0xFFFFFFFFu, ok);
           if (!ok) break;
           ptx::tc_fence_after();
-          uint8_t* a_st = sA + stage * Cfg::kStageA;
-          uint8_t* b_st = sB + stage * Cfg::kStageB;
-          if (lane == 0) {
-            const uint32_t a_addr = ptx::smem_addr(a_st);
-            const uint32_t b_addr = ptx::smem_addr(b_st);
-            // one 16-deep K step of the block into the accumulator
-            auto mma_step = [&](int kk, uint32_t accum) {
-              const uint64_t adesc = a_mn ? ptx::sw128_desc(a_addr + kk * 2048, kBK * 128, 1024)
-                                          : ptx::sw128_desc(a_addr + kk * 32, 16, 1024);
-              const uint64_t bdesc = b_mn ? ptx::sw128_desc(b_addr + kk * 2048, b_lbo, 1024)
-                                          : ptx::sw128_desc(b_addr + kk * 32, 16, 1024);
-              if (PAIR) ptx::tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, accum);
-              else ptx::tc_mma_bf16(d_tmem, adesc, bdesc, idesc, accum);
-            };
-            if (kk0 == 0) {
-              // every block but a dw group's straddling last one: four MMAs back to
-              // back (with a skip test in front of each, dw's issue took ~1.3x as long)
+          const uint32_t a_addr = ptx::smem_addr(sA + stage * Cfg::kStageA);
+          const uint32_t b_addr = ptx::smem_addr(sB + stage * Cfg::kStageB);
+          // one 16-deep K step of the block into the accumulator
+          auto mma_step = [&](int kk, uint32_t accum) {
+            const uint64_t adesc = a_mn ? ptx::sw128_desc(a_addr + kk * 2048, kBK * 128, 1024)
+                                        : ptx::sw128_desc(a_addr + kk * 32, 16, 1024);
+            const uint64_t bdesc = b_mn ? ptx::sw128_desc(b_addr + kk * 2048, b_lbo, 1024)
+                                        : ptx::sw128_desc(b_addr + kk * 32, 16, 1024);
+            if (PAIR) ptx::tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, accum);
+            else ptx::tc_mma_bf16(d_tmem, adesc, bdesc, idesc, accum);
+          };
+          if (kk0 == 0) {
+            // every block but a dw group's straddling last one: four MMAs back to
+            // back (with a skip test in front of each, dw's issue took ~1.3x as long)
 #pragma unroll
-              for (int kk = 0; kk < kBK / 16; ++kk) mma_step(kk, (kb > 0 || kk > 0) ? 1u : 0u);
-            } else {
+            for (int kk = 0; kk < kBK / 16; ++kk) mma_step(kk, (kb > 0 || kk > 0) ? 1u : 0u);
+          } else {
 #pragma unroll 1
-              for (int kk = kk0; kk < kBK / 16; ++kk) mma_step(kk, (kb > 0 || kk > kk0) ? 1u : 0u);
-            }
-            if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&sh.empty[stage]), 0x3);
-            else ptx::tc_commit(ptx::smem_addr(&sh.empty[stage]));
+            for (int kk = kk0; kk < kBK / 16; ++kk) mma_step(kk, (kb > 0 || kk > kk0) ? 1u : 0u);
           }
-          __syncwarp();
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1;
-          }
+          if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&sh.empty[stage]), 0x3);
+          else ptx::tc_commit(ptx::smem_addr(&sh.empty[stage]));
+          if (++stage == S) stage = 0;
         }
         if (!ok) break;
-        if (lane == 0) {
-          if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&sh.tfull[acc]), 0x3);
-          else ptx::tc_commit(ptx::smem_addr(&sh.tfull[acc]));
-        }
-        __syncwarp();
+        if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&sh.tfull[acc]), 0x3);
+        else ptx::tc_commit(ptx::smem_addr(&sh.tfull[acc]));
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
       if (*abort_flag) {
         // wait until every MMA this thread issued has completed before TMEM is freed
-        if (lane == 0) {
-          volatile int no_abort = 0;
-          if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&sh.drain), 0x1);
-          else ptx::tc_commit(ptx::smem_addr(&sh.drain));
-          ptx::mbar_wait_bounded(ptx::smem_addr(&sh.drain), 0, &no_abort, kDrainNs);
-        }
-        __syncwarp();
+        volatile int no_abort = 0;
+        if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&sh.drain), 0x1);
+        else ptx::tc_commit(ptx::smem_addr(&sh.drain));
+        ptx::mbar_wait_bounded(ptx::smem_addr(&sh.drain), 0, &no_abort, kDrainNs);
       }
     }
+    __syncwarp();
   } else if (warp < 2 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     // Eight warps, two per 32-lane quarter of the accumulator (32 tile rows);
