@@ -44,7 +44,7 @@ def _call(rd, op, a, w, do, gs, status):
 
 
 @pytest.mark.parametrize("variant,op", [("single", "fwd"), ("pair", "fwd"), ("single", "dx"),
-                                        ("pair", "dx"), ("single", "dw")])
+                                        ("pair", "dx"), ("single", "dw"), ("pair", "dw")])
 def test_timeout_unwinds_and_reports(rd_lib, monkeypatch, variant, op):
     monkeypatch.setenv("RD_GEMM_VARIANT", variant)
     a, w, do, sizes = _inputs(op, 1)
