@@ -782,10 +782,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Rows [0, zero_lo) and [zero_hi, L) are two contiguous byte ranges of the
     // output (its rows are contiguous).  Each CTA takes a contiguous 16-byte
     // aligned share of their concatenation and has the bulk-copy engine write it
-    // from a 4 KB zero block in shared memory.  The writes are paced by the
-    // CTA's own progress: the bytes issued follow the stages the producer has
-    // filled, reaching the whole share at 4/5 of them, so that they spread over
-    // the run instead of meeting the operand reads in HBM in one burst.
+    // from a 4 KB zero block in shared memory.  Units (CTAs or CTA pairs) with
+    // one tile fewer than the others take twice the share: they have a tile's
+    // time to spare at the end.  The writes are paced by the CTA's own progress
+    // (the bytes issued follow the stages its producer has filled), so that they
+    // spread over the run instead of meeting the operand reads in HBM in one burst.
     for (int i = lane; i < 256; i += 32) sh.zeros[i] = make_uint4(0, 0, 0, 0);
     ptx::fence_proxy_async_smem();
     __syncwarp();
@@ -794,8 +795,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t lo_bytes = static_cast<uint64_t>(sh.zero_lo) * row_bytes;
       const uint64_t z_bytes = lo_bytes + static_cast<uint64_t>(sh.L - sh.zero_hi) * row_bytes;
       const uint64_t units16 = z_bytes / 16;
-      const uint64_t u0 = units16 * blockIdx.x / gridDim.x;
-      const uint64_t u1 = units16 * (blockIdx.x + 1) / gridDim.x;
+      // weight of a unit: 1, or 2 for the units with one tile fewer (u >= r);
+      // W(u) = total weight of the units before u
+      const int r = total % units;
+      auto W = [&](int u) -> uint64_t {
+        return (r == 0 || u <= r) ? static_cast<uint64_t>(u) : static_cast<uint64_t>(r + 2 * (u - r));
+      };
+      const uint64_t wt = W(units);
+      const uint64_t a0 = units16 * W(unit) / wt, a1 = units16 * W(unit + 1) / wt;
+      const uint64_t per_unit = PAIR ? 2 : 1, sub = PAIR ? (blockIdx.x & 1u) : 0;
+      const uint64_t u0 = a0 + (a1 - a0) * sub / per_unit;
+      const uint64_t u1 = a0 + (a1 - a0) * (sub + 1) / per_unit;
       if (u1 > u0) {
         int64_t stages = 0;  // stages this CTA's producer fills in all
         for (int t = unit; t < total; t += units) stages += decode_tile<OP, PAIR>(sh, args, t).nkb;
@@ -808,10 +818,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         while (done < share) {
           const int64_t f = *fills;
-          const uint64_t target =
-              (stages == 0 || 5 * f >= 4 * stages)
-                  ? share
-                  : share * static_cast<uint64_t>(5 * f) / static_cast<uint64_t>(4 * stages);
+          const uint64_t target = (stages == 0 || f >= stages)
+                                      ? share
+                                      : share * static_cast<uint64_t>(f) / static_cast<uint64_t>(stages);
           if (target <= done) {
             // pacing only: give up (and unwind with the CTA) like any other wait
             if (*abort_flag) break;
