@@ -16,17 +16,18 @@
 //     boundaries (exclusive prefix clamped to L) and the per-group tile
 //     prefix in shared memory -- no workspace, no host round trip;
 //   * tiles are handed out by static striding over (group, band, n-tile,
-//     m-tile): within a band of rows (4096 by default) the m-tiles run fastest, so the CTAs
-//     working at one time share each rhs column panel through L2 and the
-//     band's lhs rows stay in L2 until every column panel has used them;
+//     m-tile): within a band of rows (4096 by default) the m-tiles run
+//     fastest, so the CTAs working at one time share each rhs column panel
+//     through L2 and the band's lhs rows stay in L2 until every column panel
+//     has used them;
 //   * warp 0 (one lane) streams A/B blocks with TMA into a ring of
-//     128-byte-swizzled tiles; warp 1 issues tcgen05.mma into one of two
-//     TMEM accumulators; warps 2-9 (two per TMEM lane quarter) drain the other
-//     accumulator with
+//     128-byte-swizzled tiles; one lane of warp 1 waits for each block,
+//     issues its tcgen05.mma into one of two TMEM accumulators and commits;
+//     warps 2-9 (two per TMEM lane quarter) drain the other accumulator with
 //     tcgen05.ld, round to bf16 (or apply the GLU) and store full 64-byte row
 //     segments through a small shared-memory transpose, with row masks;
 //     warp 10 has the bulk-copy engine write the zero rows of the forward/dx
-//     outputs from a zero block in shared memory;
+//     outputs from a zero block in shared memory, paced by the producer;
 //   * PAIR=false: one CTA per SM computes a 128x256 tile (UMMA 128x256x16,
 //     4-stage ring of 48 KB).  PAIR=true: a cluster of two CTAs computes a
 //     256x256 tile with the CTA-pair UMMA (cta_group::2, 256x256x16): each
