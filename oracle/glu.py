@@ -12,11 +12,11 @@ Two forms of each:
 * ``*_f64`` -- the mathematical value in float64 (what results are compared
   against, with a bf16-ulp tolerance);
 * ``*_f32`` -- the float32 op sequence that the page fixes for the forward
-  and that this build fixes for the backward (the page gives no backward
+  and that this library fixes for the backward (the page gives no backward
   formula), rounded once to bf16.  It defines the special values (NaN, +-inf,
   signed zeros) that the GPU must reproduce bit for bit.
 
-Readings (listed in the design doc): silu(g) = g / (1 + exp(-g)) with a single
+Readings: silu(g) = g / (1 + exp(-g)) with a single
 divide; the backward uses sig = 1/(1+exp(-g)), d_up = d * silu(g) and
 d_gate = (d*u) * (sig * (1 + g*(1 - sig))); the "-0 -> +0 fix" turns every
 backward output that rounds to -0 into +0.  ``exp`` in the f32 form is the

@@ -14,7 +14,7 @@ Sources:
   commit message: only rows [0, limit) of the packed buffer hold tokens; the
   grouped matmuls skip the rest, and rows left unwritten are never read.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 
 * L = min(limit, m) (limit absent => m).  Group boundaries are the exclusive
   prefix of the sizes, negative sizes taken as 0, every boundary clamped to L.

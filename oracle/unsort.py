@@ -8,10 +8,10 @@ f32 routing-weight row dot dot[r] = sum_c f32(g[r, c]) * f32(y[r, c]), where g
 is the gathered output gradient, y the sorted tokens and w the per-row
 routing weight.
 
-Readings (listed in the design doc): rows at or past L = min(limit, rows) are
+Readings: rows at or past L = min(limit, rows) are
 neither read nor written (the page's TPU kernel also zeroes the rest of
-limit's 1024-row block, an artefact of its blocking that this build does not
-copy); the dot is compared in float64 with the worst-case bound of any f32
+limit's 1024-row block, an artefact of its blocking that this library does
+not copy); the dot is compared in float64 with the worst-case bound of any f32
 summation order, since each product of two bf16 values is exact in f32.
 """
 from __future__ import annotations
