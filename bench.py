@@ -348,7 +348,17 @@ def run_ops(rd, device, stream, peaks):
         B = w.m * w.k * 2 + w.m * w.n * 2 + w.g_total * w.k * w.n * 2
         res["dw"] = {"us": t * 1e6, "tflops": F / t / 1e12, "bound": "tensor",
                      "frac": max(F / P, B / BW) / t}
-        del x, do, wt, dx, dw
+        del dx, dw
+        torch.cuda.empty_cache()
+        # dw kept in f32 (stored, then added into an existing gradient buffer)
+        dw32 = torch.zeros((w.g_total, w.k, w.n), dtype=torch.float32, device=device)
+        for key, acc in (("dw_f32", False), ("dw_f32_accumulate", True)):
+            t = med(lambda: rd.trans_ragged_dot_f32(x, do, gs, out=dw32, accumulate=acc), entry=key)
+            B = w.m * w.k * 2 + w.m * w.n * 2 + w.g_total * w.k * w.n * 4 * (2 if acc else 1)
+            res[key] = {"us": t * 1e6, "tflops": F / t / 1e12,
+                        "bound": "tensor" if F / P >= B / BW else "hbm",
+                        "frac": max(F / P, B / BW) / t}
+        del x, do, wt, dw32
         torch.cuda.empty_cache()
 
         # decode pair (up with GLU, down) sharing group_sizes inside one CUDA graph

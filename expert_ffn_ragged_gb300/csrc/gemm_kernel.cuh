@@ -616,6 +616,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         float* outf = reinterpret_cast<float*>(args.out) +
                       static_cast<size_t>(tl.j) * args.m_out * args.ldo;
+        // the accumulating form reads the prior values of all four rows before it
+        // writes any (one read-modify-write after another serialised four HBM
+        // round trips)
+        uint4 prior[4];
+        if (EPI == kEpiF32Acc) {
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int row = wrow0 + it * 8 + sr;
+            const int c = col + piece * 4;
+            prior[it] = (row < hi && c + 4 <= args.n_out)
+                            ? *reinterpret_cast<const uint4*>(outf + static_cast<size_t>(row) * args.ldo + c)
+                            : make_uint4(0, 0, 0, 0);
+          }
+        }
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
           const int rl = it * 8 + sr;
@@ -625,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (row < hi && c + 4 <= args.n_out) {
             uint4* dst = reinterpret_cast<uint4*>(outf + static_cast<size_t>(row) * args.ldo + c);
             if (EPI == kEpiF32Acc) {
-              const uint4 o = *dst;
+              const uint4 o = prior[it];
               val = make_uint4(__float_as_uint(__fadd_rn(__uint_as_float(o.x), __uint_as_float(val.x))),
                                __float_as_uint(__fadd_rn(__uint_as_float(o.y), __uint_as_float(val.y))),
                                __float_as_uint(__fadd_rn(__uint_as_float(o.z), __uint_as_float(val.z))),
@@ -650,6 +664,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         continue;
+      }
+      if (EPI == kEpiF32Acc) {
+        // the prior values this lane will add to (its row, this warp's columns) do not
+        // depend on the accumulator: bring them into L2 while the MMAs run
+        const int row = wrow0 + lane;
+        if (row < hi) {
+          const float* rp = reinterpret_cast<const float*>(args.out) +
+                            (static_cast<size_t>(tl.j) * args.m_out + row) * args.ldo;
+#pragma unroll
+          for (int c = c_begin * 32; c < c_end * 32; c += 32)  // 32 floats = 128 bytes
+            if (col0 + c < args.n_out) ptx::prefetch_l2(rp + col0 + c);
+        }
       }
       bool ok = ptx::mbar_wait_bounded(ptx::smem_addr(&sh.tfull[acc]), acc_phase, abort_flag,
                                        tlimit);

@@ -133,6 +133,11 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
 }
 
 // ---------------------------------------------------------------- TMA
+// bring the line holding `p` into L2 (a hint: no data returns, nothing waits)
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
