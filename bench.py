@@ -17,11 +17,16 @@ Also reported on the same line:
   cpu_baseline  the float64 oracle timed on a bounded sample of the same
                 workload on this host's cores;
   ops           the other rows of the hot path at their own workloads
-                (packed GLU forward, dx, dw, decode pair in one CUDA graph,
-                standalone GLU forward/backward, unsort backward, the fused
-                GLU backward through the down projection, and the expert FFN
-                forward graph from 256 to 16384 tokens), each as time per call
-                and fraction of its roofline.
+                (packed GLU forward, dx, dw in bf16, f32 and accumulating
+                f32, decode pair in one CUDA graph, standalone GLU
+                forward/backward, unsort backward, the fused GLU backward
+                through the down projection, the tiny workload's latency, and
+                the expert FFN forward graph from 256 to 16384 tokens), each as
+                time per call (median, p10, p90) and fraction of its roofline.
+
+--profile NAME runs a few launches of one workload for ncu (mixtral,
+mixtral_small, packed_glu, dx, dw, dw_f32acc, packed_dx_glu_bwd, glu_fwd,
+glu_bwd, unsort, decode).
 
 --impl reference times the oracle itself as the reference arm.
 Under torchrun (--gpus N) every rank runs an independent replica (no
@@ -747,11 +752,15 @@ def run_profile(args):
         lim = torch.tensor([w.limit], dtype=torch.int32, device=device)
         out = torch.empty((w.m, w.n // 2), dtype=torch.bfloat16, device=device)
         fn = lambda: rd.ragged_dot(lhs, rhs, gs, w.group_offset, lim, rd.EPI_SILU_GLU, out)
-    elif name in ("dx", "dw"):
+    elif name in ("dx", "dw", "dw_f32acc"):
         w = workloads.backward_pair()
         gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=device)
         do = normal_bf16((w.m, w.n), 1.0, 41, device)
-        if name == "dx":
+        if name == "dw_f32acc":
+            x = normal_bf16((w.m, w.k), 1.0, 40, device)
+            dw32 = torch.zeros((w.g_total, w.k, w.n), dtype=torch.float32, device=device)
+            fn = lambda: rd.trans_ragged_dot_f32(x, do, gs, out=dw32, accumulate=True)
+        elif name == "dx":
             wt = normal_bf16((w.g_total, w.k, w.n), w.rhs_var, 42, device)
             dx = torch.empty((w.m, w.k), dtype=torch.bfloat16, device=device)
             fn = lambda: rd.ragged_dot_trans_rhs(do, wt, gs, out=dx)
