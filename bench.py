@@ -359,7 +359,10 @@ def run_ops(rd, device, stream, peaks):
         dw32 = torch.zeros((w.g_total, w.k, w.n), dtype=torch.float32, device=device)
         for key, acc in (("dw_f32", False), ("dw_f32_accumulate", True)):
             t = med(lambda: rd.trans_ragged_dot_f32(x, do, gs, out=dw32, accumulate=acc), entry=key)
-            B = w.m * w.k * 2 + w.m * w.n * 2 + w.g_total * w.k * w.n * 4 * (2 if acc else 1)
+            # storing writes every block (empty groups' as zeros); accumulating reads
+            # and writes only the blocks of groups with rows
+            B = w.m * w.k * 2 + w.m * w.n * 2 + (live * w.k * w.n * 4 * 2 if acc
+                                                 else w.g_total * w.k * w.n * 4)
             res[key] = {"us": t * 1e6, "tflops": F / t / 1e12,
                         "bound": "tensor" if F / P >= B / BW else "hbm",
                         "frac": max(F / P, B / BW) / t}
