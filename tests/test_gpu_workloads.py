@@ -267,3 +267,93 @@ def test_expert_ffn_chain_in_one_graph(rd_lib, tokens):
         ref = h64[sel] @ _f64(down[j][:, ocidx])
         assert_close(got_o[sel], ref, gemm_tol(ref, F, h_amax, d_amax),
                      f"ffn {tokens} down group {j}")
+
+
+def test_backward_pair_dw_f32_full_size(rd_lib):
+    """dw kept in f32 at the backward-pair size: stored, and accumulated into a prior buffer.
+
+    Sampled (k, n) entries of every group against float64, within the worst-case
+    error of an f32 sum of the exact products (plus one f32 rounding for the
+    accumulating add); groups without rows are zero when stored and keep their
+    prior block when accumulated.
+    """
+    from workloads import backward_pair, normal_bf16
+
+    w = backward_pair()
+    x = normal_bf16((w.m, w.k), 1.0, 40, DEV)
+    do = normal_bf16((w.m, w.n), 1.0, 41, DEV)
+    gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=DEV)
+    gen = torch.Generator(device=DEV).manual_seed(44)
+    prior = torch.randn((w.g_total, w.k, w.n), generator=gen, device=DEV)
+    stored = rd_lib.trans_ragged_dot_f32(x, do, gs)
+    acc = prior.clone()
+    rd_lib.trans_ragged_dot_f32(x, do, gs, out=acc, accumulate=True)
+    torch.cuda.synchronize()
+    b, _ = oracle.group_bounds(w.group_sizes, w.m)
+    rng = np.random.default_rng(5)
+    kk = torch.from_numpy(_sample_cols(w.k, rng, 40, tile=128)).to(DEV)
+    nn = torch.from_numpy(_sample_cols(w.n, rng, 40)).to(DEV)
+    for j in range(w.g_total):
+        lo, hi = int(b[j]), int(b[j + 1])
+        if hi == lo:
+            assert bool((stored[j] == 0).all()), f"empty group {j} not zero"
+            assert torch.equal(acc[j], prior[j]), f"empty group {j} changed its prior block"
+            continue
+        xs, ys = _f64(x[lo:hi][:, kk]), _f64(do[lo:hi][:, nn])
+        ref = xs.T @ ys
+        bound = (hi - lo) * 2.0 ** -23 * (np.abs(xs).T @ np.abs(ys))
+        got = stored[j][kk][:, nn].cpu().numpy().astype(np.float64)
+        assert_close(got, ref, bound, f"dw f32 group {j}")
+        p64 = prior[j][kk][:, nn].cpu().numpy().astype(np.float64)
+        want = p64 + ref
+        tol = bound + np.abs(np.spacing(want.astype(np.float32))).astype(np.float64)
+        got = acc[j][kk][:, nn].cpu().numpy().astype(np.float64)
+        assert_close(got, want, tol, f"dw f32 accumulated group {j}")
+
+
+def test_packed_dx_glu_bwd_full_size(rd_lib):
+    """dx of the down projection with the GLU backward fused, on the packed buffer.
+
+    [225280, 4096] output gradient, experts 16..31 of 64 with down weights
+    [16, 1024, 4096], the saved [gate | up] rows, limit 126156 -- the launch the
+    bench times.  Rows past the limit keep their sentinel, rows below it outside
+    the local groups are +0 (both checked on the device), and sampled rows x
+    columns of every local group match float64 within the fused-epilogue bound.
+    """
+    from oracle import glu as oglu
+    from workloads import normal_bf16, packed_glu_fwd
+
+    w = packed_glu_fwd()
+    f, n = 1024, 4096
+    gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=DEV)
+    lim = torch.tensor([w.limit], dtype=torch.int32, device=DEV)
+    d_out = normal_bf16((w.m, n), 1.0, 35, DEV)
+    w_down = normal_bf16((w.g_local, f, n), 1.0 / n, 36, DEV)
+    fused = normal_bf16((w.m, 2 * f), 1.0, 37, DEV)
+    out = torch.empty((w.m, 2 * f), dtype=torch.bfloat16, device=DEV)
+    out.view(torch.int16).fill_(SENT)
+    rd_lib.ragged_dot_trans_rhs_glu_bwd(d_out, w_down, fused, gs, w.group_offset, lim, out)
+    torch.cuda.synchronize()
+    b, L = oracle.group_bounds(w.group_sizes, w.m, w.limit)
+    lo_all, hi_all = int(b[w.group_offset]), int(b[w.group_offset + w.g_local])
+    assert bool((out[L:].view(torch.int16) == SENT).all()), "a row past the limit was written"
+    assert bool((out[:lo_all].view(torch.int16) == 0).all()), "rows before the shard are not +0"
+    assert bool((out[hi_all:L].view(torch.int16) == 0).all()), "rows after the shard are not +0"
+    rng = np.random.default_rng(6)
+    rows = _sample_rows(b, w.group_offset, w.group_offset + w.g_local, rng, per_group=3)
+    ridx = torch.from_numpy(rows).to(DEV)
+    cols = _sample_cols(f, rng, 64, tile=128)
+    cidx = torch.from_numpy(cols).to(DEV)
+    d64 = _f64(d_out[ridx])
+    g64, u64 = _f64(fused[ridx][:, cidx]), _f64(fused[ridx][:, cidx + f])
+    got_g, got_u = _f64(out[ridx][:, cidx]), _f64(out[ridx][:, cidx + f])
+    E = 1e-3 * math.sqrt(n) * float(d_out[lo_all:hi_all].float().abs().max()) * \
+        float(w_down.float().abs().max())
+    grp = _group_of(rows, b) - w.group_offset
+    for j in np.unique(grp):
+        sel = np.nonzero(grp == j)[0]
+        dh = d64[sel] @ _f64(w_down[j][cidx]).T
+        ref_g, ref_u = oglu.glu_bwd_f64(g64[sel], u64[sel], dh)
+        dg1, du1 = oglu.glu_bwd_f64(g64[sel], u64[sel], 1.0)
+        assert_close(got_g[sel], ref_g, obf.ulp(ref_g) + np.abs(dg1) * E, f"d_gate group {j}")
+        assert_close(got_u[sel], ref_u, obf.ulp(ref_u) + np.abs(du1) * E, f"d_up group {j}")
