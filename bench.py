@@ -22,7 +22,10 @@ Also reported on the same line:
                 forward/backward, unsort backward, the fused GLU backward
                 through the down projection, the tiny workload's latency, and
                 the expert FFN forward graph from 256 to 16384 tokens), each as
-                time per call (median, p10, p90) and fraction of its roofline.
+                median time per call in us, fraction of its roofline and the
+                bound ("t" tensor, "h" HBM, "l" latency), with p10 / p90 for
+                the five configs; short keys and 3-4 significant digits keep
+                the whole line short.  --ops-json FILE writes the full figures.
 
 --profile NAME runs a few launches of one workload for ncu (mixtral,
 mixtral_small, packed_glu, dx, dw, dw_f32acc, packed_dx_glu_bwd, glu_fwd,
@@ -283,7 +286,8 @@ def run_ops(rd, device, stream, peaks):
         t = med(lambda: rd.ragged_dot(lhs, rhs, gs, w.group_offset, lim, rd.EPI_SILU_GLU, out),
                 entry="packed_glu_fwd")
         res["packed_glu_fwd"] = {"us": t * 1e6, "tflops": F / t / 1e12, "gbs": B / t / 1e9,
-                                 "bound": "tensor", "frac": max(F / P, B / BW) / t,
+                                 "bound": "hbm" if B / BW > F / P else "tensor",
+                                 "frac": max(F / P, B / BW) / t,
                                  "local_rows": rows, "zero_rows": zero_rows}
         # standalone GLU on the same packed buffer shape
         fused = normal_bf16((w.m, 2 * 1024), 1.0, 32, device)
@@ -347,11 +351,13 @@ def run_ops(rd, device, stream, peaks):
         live = int((w.group_sizes > 0).sum())
         t = med(lambda: rd.ragged_dot_trans_rhs(do, wt, gs, out=dx), entry="dx")
         B = w.m * w.n * 2 + live * w.k * w.n * 2 + w.m * w.k * 2
-        res["dx"] = {"us": t * 1e6, "tflops": F / t / 1e12, "bound": "tensor",
+        res["dx"] = {"us": t * 1e6, "tflops": F / t / 1e12,
+                     "bound": "hbm" if B / BW > F / P else "tensor",
                      "frac": max(F / P, B / BW) / t}
         t = med(lambda: rd.trans_ragged_dot(x, do, gs, out=dw), entry="dw")
         B = w.m * w.k * 2 + w.m * w.n * 2 + w.g_total * w.k * w.n * 2
-        res["dw"] = {"us": t * 1e6, "tflops": F / t / 1e12, "bound": "tensor",
+        res["dw"] = {"us": t * 1e6, "tflops": F / t / 1e12,
+                     "bound": "hbm" if B / BW > F / P else "tensor",
                      "frac": max(F / P, B / BW) / t}
         del dx, dw
         torch.cuda.empty_cache()
@@ -433,6 +439,62 @@ def run_ops(rd, device, stream, peaks):
             res[entry][prefix + "p10_us"] = p10
             res[entry][prefix + "p90_us"] = p90
     return res
+
+
+def _sig(x, digits=4):
+    """x rounded to `digits` significant digits (keeps the JSON line short)."""
+    if x is None or x == 0:
+        return x
+    return float(f"{x:.{digits}g}")
+
+
+def compact_ops(res):
+    """The ops as a short dict: time (us), roofline fraction and bound of every row.
+
+    Keys name the row and its workload: c1 tiny, c3 packed GLU forward, c4 the
+    backward pair (dx, dw, dw in f32, accumulated f32), c5 the decode pair in one
+    graph (skewed / uniform routing), the standalone GLU and unsort passes on the
+    packed buffer, the fused dx + GLU backward, and the expert-FFN graph by token
+    count ([us, frac, bound]).  p10 / p90 are given for the five configs.
+    """
+    b = {"tensor": "t", "hbm": "h", "latency": "l"}
+    out = {}
+
+    def row(key, src, us_key="us", frac_key="frac", spread_prefix="", extra=()):
+        if src not in res:
+            return
+        r = res[src]
+        e = {"us": _sig(r[us_key]), "frac": _sig(r.get(frac_key), 3)}
+        if "bound" in r:
+            e["b"] = b.get(r["bound"], r["bound"])
+        p10, p90 = r.get(spread_prefix + "p10_us"), r.get(spread_prefix + "p90_us")
+        if key.startswith("c") and p10 is not None:
+            e["p10"], e["p90"] = _sig(p10, 3), _sig(p90, 3)
+        for k_out, k_in in extra:
+            e[k_out] = _sig(r[k_in])
+        out[key] = e
+
+    if "tiny" in res:
+        t = res["tiny"]
+        out["c1_tiny"] = {"us": _sig(t["us"], 3), "call_us": _sig(t["call_us"], 3),
+                          "p10": _sig(t.get("call_p10_us"), 3), "p90": _sig(t.get("call_p90_us"), 3),
+                          "b": "l"}
+    row("c3_glu_fwd", "packed_glu_fwd")
+    row("c4_dx", "dx")
+    row("c4_dw", "dw")
+    row("c4_dw_f32", "dw_f32")
+    row("c4_dw_f32_acc", "dw_f32_accumulate")
+    for key, src in (("c5_skew", "decode_skewed"), ("c5_unif", "decode_uniform")):
+        row(key, src, us_key="graph_pair_us", frac_key="pair_frac", spread_prefix="graph_pair_",
+            extra=(("up_us", "up_us"), ("down_us", "down_us")))
+    row("glu_fwd", "glu_fwd")
+    row("glu_bwd", "glu_bwd")
+    row("dx_glu_bwd", "packed_dx_glu_bwd", extra=(("unfused_us", "unfused_us"),))
+    row("unsort", "unsort_bwd_rows")
+    if "ffn_sweep" in res:
+        out["ffn"] = {str(r["tokens"]): [_sig(r["us"]), _sig(r["frac"], 3), b[r["bound"]]]
+                      for r in res["ffn_sweep"]}
+    return out
 
 
 def ffn_sweep(rd, device, stream, peaks, tokens=(256, 1024, 4096, 16384)):
@@ -674,7 +736,11 @@ def run_rd(args):
 
     ops = None
     if not args.no_ops and rank == 0:
-        ops = run_ops(rd, device, stream, peaks)
+        detail = run_ops(rd, device, stream, peaks)
+        if args.ops_json:
+            with open(args.ops_json, "w") as f:
+                json.dump(detail, f, indent=1)
+        ops = compact_ops(detail)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -700,21 +766,20 @@ def run_rd(args):
                        "valid_rows": rows, "group_sizes": w.group_sizes.tolist(),
                        "l2": "inputs larger than L2 (2.15 GB per step), no flush",
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": traffic,
+            "roofline": {"bound": "tensor", "achieved": _sig(achieved, 5), "peak": peak,
+                         "unit": "TFLOP/s", "frac": _sig(achieved / peak, 4), "traffic": traffic,
                          "peak_source": f"{peak_src} bf16_tflops (burst)",
                          "algorithmic_bytes": alg_bytes,
                          "kernel": "grouped_gemm_kernel<fwd>"},
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+            "e2e": {"value": _sig(e2e_value, 5), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                     "pipelined": "upload i+1 / forward i / download i-1 on three streams",
-                    "bound": {"h2d_gbs": h2d_gbs, "d2h_gbs": d2h_gbs,
-                              "measured": "step's upload and download, concurrent",
-                              "limit": e2e_limit, "frac": e2e_value / e2e_limit}},
+                    "bound": {"h2d_gbs": _sig(h2d_gbs), "d2h_gbs": _sig(d2h_gbs),
+                              "limit": _sig(e2e_limit), "frac": _sig(e2e_value / e2e_limit, 3)}},
             "gpu_launches": args.steps,
-            "launch_ms": {"median": statistics.median(per),
-                          "p10": statistics.quantiles(per, n=10)[0] if len(per) > 1 else per[0],
-                          "p90": statistics.quantiles(per, n=10)[-1] if len(per) > 1 else per[0]},
+            "launch_ms": {"median": _sig(statistics.median(per), 5),
+                          "p10": _sig(statistics.quantiles(per, n=10)[0] if len(per) > 1 else per[0], 5),
+                          "p90": _sig(statistics.quantiles(per, n=10)[-1] if len(per) > 1 else per[0], 5)},
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
             "ops": ops,
@@ -828,6 +893,8 @@ def main():
     ap.add_argument("--no-ops", action="store_true", help="skip the other hot-path rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None, help="run only a few launches of a workload (for ncu)")
+    ap.add_argument("--ops-json", default=None,
+                    help="also write the other rows' full timings (p10/p90, GB/s, TFLOP/s) to this file")
     args = ap.parse_args()
     if args.warmup < 3 and args.profile is None:
         args.warmup = 3

@@ -15,6 +15,12 @@ Functions (same names as the C ABI, without the ``rd_`` prefix):
 * ``glu_fwd(fused, limit=None)``                         -> out [rows, f]
 * ``glu_bwd(fused, d_out, limit=None)``                  -> d_fused [rows, 2f]
 * ``unsort_bwd_rows(g, y, w, limit=None)``                -> (grad [rows, hidden], dot [rows])
+* ``set_tuning(...)``, ``get_tuning()``, ``tuning(...)``  -> the process-wide launch overrides
+
+Every tensor of a call must sit on one CUDA device; the call runs on that
+device's current stream (or ``stream``).  A ``status`` word (a one-element
+int32 CUDA tensor) collects the device-side status bits; without one a call
+whose bounded waits ran out cannot be told from a completed one.
 """
 from __future__ import annotations
 
@@ -27,6 +33,7 @@ __all__ = [
     "trans_ragged_dot", "trans_ragged_dot_f32",
     "glu_fwd", "glu_bwd", "unsort_bwd_rows", "RdError", "EPI_NONE", "EPI_SILU_GLU",
     "STATUS_NEG_SIZE", "STATUS_OVERFLOW", "STATUS_TIMEOUT", "MAX_GROUPS",
+    "VARIANT_AUTO", "VARIANT_SINGLE", "VARIANT_PAIR", "set_tuning", "get_tuning", "tuning",
 ]
 
 EPI_NONE = 0
@@ -35,10 +42,18 @@ STATUS_NEG_SIZE = 1
 STATUS_OVERFLOW = 2
 STATUS_TIMEOUT = 4
 MAX_GROUPS = 1024
+VARIANT_AUTO = 0
+VARIANT_SINGLE = 1
+VARIANT_PAIR = 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "librd.so")
 _lib = None
+
+
+class _Tuning(ctypes.Structure):
+    _fields_ = [("gemm_variant", ctypes.c_int32), ("band_rows", ctypes.c_int32),
+                ("wait_timeout_ns", ctypes.c_uint64)]
 
 
 class RdError(RuntimeError):
@@ -76,6 +91,10 @@ def load():
                lib.rd_trans_ragged_dot_f32,
                lib.rd_glu_fwd, lib.rd_glu_bwd, lib.rd_unsort_bwd_rows):
         fn.restype = ctypes.c_int
+    lib.rd_set_tuning.argtypes = [ctypes.c_void_p]
+    lib.rd_get_tuning.argtypes = [ctypes.c_void_p]
+    lib.rd_set_tuning.restype = ctypes.c_int
+    lib.rd_get_tuning.restype = ctypes.c_int
     lib.rd_status_string.argtypes = [ctypes.c_int]
     lib.rd_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -92,12 +111,44 @@ def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def _stream(stream):
+def _stream(stream, device):
     import torch
 
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
+    elif stream.device != device:
+        raise ValueError("stream is on another device than the tensors")
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+class _on_device:
+    """Make ``device`` current for the call (the library launches on the current device)."""
+
+    def __init__(self, device):
+        import torch
+
+        self.idx = device.index if device.index is not None else torch.cuda.current_device()
+        self.prev = None
+
+    def __enter__(self):
+        import torch
+
+        cur = torch.cuda.current_device()
+        if cur != self.idx:
+            self.prev = cur
+            torch.cuda.set_device(self.idx)
+
+    def __exit__(self, *exc):
+        import torch
+
+        if self.prev is not None:
+            torch.cuda.set_device(self.prev)
+
+
+def _same_device(device, *tensors):
+    for t in tensors:
+        if t is not None and t.device != device:
+            raise ValueError(f"all tensors of a call must be on {device} (one is on {t.device})")
 
 
 def _bf16_2d(t, name):
@@ -131,10 +182,64 @@ def _scalar_i32(t, name):
 def _group_args(group_sizes, limit, status):
     import torch
 
-    if group_sizes.dtype != torch.int32 or group_sizes.dim() != 1 or not group_sizes.is_cuda:
-        raise ValueError("group_sizes must be a 1-D int32 CUDA tensor")
+    if (group_sizes.dtype != torch.int32 or group_sizes.dim() != 1 or not group_sizes.is_cuda
+            or not group_sizes.is_contiguous()):
+        raise ValueError("group_sizes must be a contiguous 1-D int32 CUDA tensor")
     _scalar_i32(limit, "limit")
     _scalar_i32(status, "status")
+
+
+def _fused_width(fused):
+    rows, w = fused.shape
+    if w % 2:
+        raise ValueError("fused must have an even width: [rows, 2f] = [gate | up]")
+    return rows, w // 2
+
+
+def set_tuning(variant: Optional[int] = None, band_rows: Optional[int] = None,
+               wait_timeout_ns: Optional[int] = None):
+    """Set the process-wide launch overrides of rd_set_tuning; None leaves a field as it is.
+
+    variant: VARIANT_AUTO / VARIANT_SINGLE / VARIANT_PAIR; band_rows: rows per
+    band of the forward / dx tile order (0 = default); wait_timeout_ns: bound
+    of each wait inside the kernels (0 = default).  A CUDA graph keeps the
+    values in force when it was captured.
+    """
+    lib = load()
+    cur = _Tuning()
+    _check(lib.rd_get_tuning(ctypes.byref(cur)), "rd_get_tuning")
+    if variant is not None:
+        cur.gemm_variant = int(variant)
+    if band_rows is not None:
+        cur.band_rows = int(band_rows)
+    if wait_timeout_ns is not None:
+        cur.wait_timeout_ns = int(wait_timeout_ns)
+    _check(lib.rd_set_tuning(ctypes.byref(cur)), "rd_set_tuning")
+
+
+def get_tuning() -> dict:
+    lib = load()
+    cur = _Tuning()
+    _check(lib.rd_get_tuning(ctypes.byref(cur)), "rd_get_tuning")
+    return {"variant": cur.gemm_variant, "band_rows": cur.band_rows,
+            "wait_timeout_ns": cur.wait_timeout_ns}
+
+
+class tuning:
+    """Context manager: the overrides of ``set_tuning`` inside, the previous values after."""
+
+    def __init__(self, **kw):
+        self.kw = kw
+        self.saved = None
+
+    def __enter__(self):
+        self.saved = get_tuning()
+        set_tuning(**self.kw)
+        return self
+
+    def __exit__(self, *exc):
+        s = self.saved
+        set_tuning(s["variant"], s["band_rows"], s["wait_timeout_ns"])
 
 
 def ragged_dot(lhs, rhs, group_sizes, group_offset: int = 0, limit=None, epilogue: int = EPI_NONE,
@@ -151,12 +256,15 @@ def ragged_dot(lhs, rhs, group_sizes, group_offset: int = 0, limit=None, epilogu
     if k2 != k:
         raise ValueError("lhs and rhs disagree on k")
     n_out = n // 2 if epilogue == EPI_SILU_GLU else n
+    dev = lhs.device
     if out is None:
-        out = torch.empty((m, n_out), dtype=torch.bfloat16, device=lhs.device)
+        out = torch.empty((m, n_out), dtype=torch.bfloat16, device=dev)
     _out(out, (m, n_out), torch.bfloat16)
-    code = lib.rd_ragged_dot(_ptr(lhs), _ptr(rhs), _ptr(out), m, k, n, _ptr(group_sizes),
-                             group_sizes.numel(), group_offset, g_local, _ptr(limit),
-                             int(epilogue), _ptr(status), _stream(stream))
+    _same_device(dev, rhs, out, group_sizes, limit, status)
+    with _on_device(dev):
+        code = lib.rd_ragged_dot(_ptr(lhs), _ptr(rhs), _ptr(out), m, k, n, _ptr(group_sizes),
+                                 group_sizes.numel(), group_offset, g_local, _ptr(limit),
+                                 int(epilogue), _ptr(status), _stream(stream, dev))
     _check(code, "rd_ragged_dot")
     return out
 
@@ -174,12 +282,15 @@ def ragged_dot_trans_rhs(lhs, rhs, group_sizes, group_offset: int = 0, limit=Non
     g_local, k, n2 = rhs.shape
     if n2 != n:
         raise ValueError("lhs and rhs disagree on n")
+    dev = lhs.device
     if out is None:
-        out = torch.empty((m, k), dtype=torch.bfloat16, device=lhs.device)
+        out = torch.empty((m, k), dtype=torch.bfloat16, device=dev)
     _out(out, (m, k), torch.bfloat16)
-    code = lib.rd_ragged_dot_trans_rhs(_ptr(lhs), _ptr(rhs), _ptr(out), m, k, n, _ptr(group_sizes),
-                                       group_sizes.numel(), group_offset, g_local, _ptr(limit),
-                                       _ptr(status), _stream(stream))
+    _same_device(dev, rhs, out, group_sizes, limit, status)
+    with _on_device(dev):
+        code = lib.rd_ragged_dot_trans_rhs(_ptr(lhs), _ptr(rhs), _ptr(out), m, k, n,
+                                           _ptr(group_sizes), group_sizes.numel(), group_offset,
+                                           g_local, _ptr(limit), _ptr(status), _stream(stream, dev))
     _check(code, "rd_ragged_dot_trans_rhs")
     return out
 
@@ -201,14 +312,31 @@ def ragged_dot_trans_rhs_glu_bwd(d_out, rhs, fused, group_sizes, group_offset: i
     g_local, f, n2 = rhs.shape
     if n2 != n or fused.shape != (m, 2 * f):
         raise ValueError("shapes disagree: d_out [m, n], rhs [g, f, n], fused [m, 2f]")
+    dev = d_out.device
     if out is None:
-        out = torch.empty((m, 2 * f), dtype=torch.bfloat16, device=d_out.device)
+        out = torch.empty((m, 2 * f), dtype=torch.bfloat16, device=dev)
     _out(out, (m, 2 * f), torch.bfloat16)
-    code = lib.rd_ragged_dot_trans_rhs_glu_bwd(
-        _ptr(d_out), _ptr(rhs), _ptr(fused), _ptr(out), m, f, n, _ptr(group_sizes),
-        group_sizes.numel(), group_offset, g_local, _ptr(limit), _ptr(status), _stream(stream))
+    _same_device(dev, rhs, fused, out, group_sizes, limit, status)
+    with _on_device(dev):
+        code = lib.rd_ragged_dot_trans_rhs_glu_bwd(
+            _ptr(d_out), _ptr(rhs), _ptr(fused), _ptr(out), m, f, n, _ptr(group_sizes),
+            group_sizes.numel(), group_offset, g_local, _ptr(limit), _ptr(status),
+            _stream(stream, dev))
     _check(code, "rd_ragged_dot_trans_rhs_glu_bwd")
     return out
+
+
+def _dw_args(x, y, group_sizes, group_offset, g_local, limit, status):
+    _bf16_2d(x, "x")
+    _bf16_2d(y, "y")
+    _group_args(group_sizes, limit, status)
+    m, k = x.shape
+    m2, n = y.shape
+    if m2 != m:
+        raise ValueError("x and y disagree on m")
+    if g_local is None:
+        g_local = group_sizes.numel() - group_offset
+    return m, k, n, g_local
 
 
 def trans_ragged_dot(x, y, group_sizes, group_offset: int = 0, g_local: Optional[int] = None,
@@ -217,48 +345,43 @@ def trans_ragged_dot(x, y, group_sizes, group_offset: int = 0, g_local: Optional
     import torch
 
     lib = load()
-    _bf16_2d(x, "x")
-    _bf16_2d(y, "y")
-    _group_args(group_sizes, limit, status)
-    m, k = x.shape
-    m2, n = y.shape
-    if m2 != m:
-        raise ValueError("x and y disagree on m")
-    if g_local is None:
-        g_local = group_sizes.numel() - group_offset
+    m, k, n, g_local = _dw_args(x, y, group_sizes, group_offset, g_local, limit, status)
+    dev = x.device
     if out is None:
-        out = torch.empty((g_local, k, n), dtype=torch.bfloat16, device=x.device)
+        out = torch.empty((g_local, k, n), dtype=torch.bfloat16, device=dev)
     _out(out, (g_local, k, n), torch.bfloat16)
-    code = lib.rd_trans_ragged_dot(_ptr(x), _ptr(y), _ptr(out), m, k, n, _ptr(group_sizes),
-                                   group_sizes.numel(), group_offset, g_local, _ptr(limit),
-                                   _ptr(status), _stream(stream))
+    _same_device(dev, y, out, group_sizes, limit, status)
+    with _on_device(dev):
+        code = lib.rd_trans_ragged_dot(_ptr(x), _ptr(y), _ptr(out), m, k, n, _ptr(group_sizes),
+                                       group_sizes.numel(), group_offset, g_local, _ptr(limit),
+                                       _ptr(status), _stream(stream, dev))
     _check(code, "rd_trans_ragged_dot")
     return out
 
 
 def trans_ragged_dot_f32(x, y, group_sizes, group_offset: int = 0, g_local: Optional[int] = None,
                          limit=None, out=None, accumulate: bool = False, status=None, stream=None):
-    """out[j] (+)= x[rows_j]^T @ y[rows_j] in f32; ``accumulate`` adds into ``out``."""
+    """out[j] (+)= x[rows_j]^T @ y[rows_j] in f32; ``accumulate`` adds into ``out``.
+
+    An accumulating call whose status reports STATUS_TIMEOUT has added some
+    tiles and not others: its output is unusable (a retry would add twice).
+    """
     import torch
 
     lib = load()
-    _bf16_2d(x, "x")
-    _bf16_2d(y, "y")
-    _group_args(group_sizes, limit, status)
-    m, k = x.shape
-    m2, n = y.shape
-    if m2 != m:
-        raise ValueError("x and y disagree on m")
-    if g_local is None:
-        g_local = group_sizes.numel() - group_offset
+    m, k, n, g_local = _dw_args(x, y, group_sizes, group_offset, g_local, limit, status)
+    dev = x.device
     if out is None:
         if accumulate:
             raise ValueError("accumulate needs an existing out buffer")
-        out = torch.empty((g_local, k, n), dtype=torch.float32, device=x.device)
+        out = torch.empty((g_local, k, n), dtype=torch.float32, device=dev)
     _out(out, (g_local, k, n), torch.float32)
-    code = lib.rd_trans_ragged_dot_f32(_ptr(x), _ptr(y), _ptr(out), m, k, n, _ptr(group_sizes),
-                                       group_sizes.numel(), group_offset, g_local, _ptr(limit),
-                                       1 if accumulate else 0, _ptr(status), _stream(stream))
+    _same_device(dev, y, out, group_sizes, limit, status)
+    with _on_device(dev):
+        code = lib.rd_trans_ragged_dot_f32(_ptr(x), _ptr(y), _ptr(out), m, k, n,
+                                           _ptr(group_sizes), group_sizes.numel(), group_offset,
+                                           g_local, _ptr(limit), 1 if accumulate else 0,
+                                           _ptr(status), _stream(stream, dev))
     _check(code, "rd_trans_ragged_dot_f32")
     return out
 
@@ -270,12 +393,14 @@ def glu_fwd(fused, limit=None, out=None, stream=None):
     lib = load()
     _bf16_2d(fused, "fused")
     _scalar_i32(limit, "limit")
-    rows, w = fused.shape
-    f = w // 2
+    rows, f = _fused_width(fused)
+    dev = fused.device
     if out is None:
-        out = torch.empty((rows, f), dtype=torch.bfloat16, device=fused.device)
+        out = torch.empty((rows, f), dtype=torch.bfloat16, device=dev)
     _out(out, (rows, f), torch.bfloat16)
-    code = lib.rd_glu_fwd(_ptr(fused), _ptr(out), rows, f, _ptr(limit), _stream(stream))
+    _same_device(dev, out, limit)
+    with _on_device(dev):
+        code = lib.rd_glu_fwd(_ptr(fused), _ptr(out), rows, f, _ptr(limit), _stream(stream, dev))
     _check(code, "rd_glu_fwd")
     return out
 
@@ -287,16 +412,18 @@ def glu_bwd(fused, d_out, limit=None, out=None, stream=None):
     lib = load()
     _bf16_2d(fused, "fused")
     _bf16_2d(d_out, "d_out")
-    rows, w = fused.shape
-    f = w // 2
+    rows, f = _fused_width(fused)
     if d_out.shape != (rows, f):
         raise ValueError("d_out must be [rows, f]")
     _scalar_i32(limit, "limit")
+    dev = fused.device
     if out is None:
-        out = torch.empty((rows, 2 * f), dtype=torch.bfloat16, device=fused.device)
+        out = torch.empty((rows, 2 * f), dtype=torch.bfloat16, device=dev)
     _out(out, (rows, 2 * f), torch.bfloat16)
-    code = lib.rd_glu_bwd(_ptr(fused), _ptr(d_out), _ptr(out), rows, f, _ptr(limit),
-                          _stream(stream))
+    _same_device(dev, d_out, out, limit)
+    with _on_device(dev):
+        code = lib.rd_glu_bwd(_ptr(fused), _ptr(d_out), _ptr(out), rows, f, _ptr(limit),
+                              _stream(stream, dev))
     _check(code, "rd_glu_bwd")
     return out
 
@@ -311,16 +438,20 @@ def unsort_bwd_rows(g, y, w, limit=None, grad=None, dot=None, stream=None):
     rows, hidden = g.shape
     if y.shape != g.shape:
         raise ValueError("g and y must have the same shape")
-    if w.dtype != torch.float32 or w.shape != (rows,) or not w.is_cuda:
-        raise ValueError("w must be a [rows] float32 CUDA tensor")
+    if (w.dtype != torch.float32 or tuple(w.shape) != (rows,) or not w.is_cuda
+            or not w.is_contiguous()):
+        raise ValueError("w must be a contiguous [rows] float32 CUDA tensor")
     _scalar_i32(limit, "limit")
+    dev = g.device
     if grad is None:
         grad = torch.empty_like(g)
     if dot is None:
-        dot = torch.empty((rows,), dtype=torch.float32, device=g.device)
+        dot = torch.empty((rows,), dtype=torch.float32, device=dev)
     _out(grad, (rows, hidden), torch.bfloat16, "grad")
     _out(dot, (rows,), torch.float32, "dot")
-    code = lib.rd_unsort_bwd_rows(_ptr(g), _ptr(y), _ptr(w), _ptr(grad), _ptr(dot), rows, hidden,
-                                  _ptr(limit), _stream(stream))
+    _same_device(dev, y, w, grad, dot, limit)
+    with _on_device(dev):
+        code = lib.rd_unsort_bwd_rows(_ptr(g), _ptr(y), _ptr(w), _ptr(grad), _ptr(dot), rows,
+                                      hidden, _ptr(limit), _stream(stream, dev))
     _check(code, "rd_unsort_bwd_rows")
     return grad, dot

@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <cstdlib>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -17,16 +17,16 @@ namespace rd {
 namespace {
 
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // default bound of any single wait in a kernel
+constexpr int32_t kBandRows = 4096;              // default rows per band of the fwd/dx tile order
 
-// Bound of each wait inside the grouped-GEMM kernels: RD_WAIT_TIMEOUT_NS when
-// set (read at every call; a test uses a tiny value to drive the timeout and
-// unwind path), else 4 s.
+// Process-wide tuning overrides (rd_set_tuning); 0 = the default.
+std::atomic<int32_t> g_variant{RD_VARIANT_AUTO};
+std::atomic<int32_t> g_band_rows{0};
+std::atomic<uint64_t> g_timeout_ns{0};
+
 uint64_t wait_timeout_ns() {
-  const char* v = getenv("RD_WAIT_TIMEOUT_NS");
-  if (v == nullptr || *v == 0) return kTimeoutNs;
-  char* end = nullptr;
-  const unsigned long long t = strtoull(v, &end, 10);
-  return (end != nullptr && *end == 0) ? static_cast<uint64_t>(t) : kTimeoutNs;
+  const uint64_t t = g_timeout_ns.load(std::memory_order_relaxed);
+  return t == 0 ? kTimeoutNs : t;
 }
 constexpr int64_t kMaxDim = 0x7FFFFFFF;
 
@@ -79,9 +79,43 @@ bool overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
   return a0 < b0 + nb && b0 < a0 + na;
 }
 
-// bf16 tensor map with 128-byte swizzle; dims/strides innermost first
+// bf16 tensor map with 128-byte swizzle; dims/strides innermost first.
+// Encoding costs about a microsecond of host time, a large share of a small
+// call, so each thread keeps the last few maps it encoded (a map is a pure
+// function of these arguments).
+struct MapKey {
+  const void* base;
+  int rank;
+  uint64_t dims[5];
+  uint64_t strides[4];
+  uint32_t box[5];
+};
+
 rd_status encode(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
                  const uint64_t* strides_bytes, const uint32_t* box) {
+  constexpr int kCache = 16;
+  struct Entry {
+    MapKey key;
+    CUtensorMap map;
+    bool valid;
+  };
+  thread_local Entry cache[kCache];
+  thread_local int next_slot = 0;
+  MapKey key;
+  std::memset(&key, 0, sizeof(key));
+  key.base = base;
+  key.rank = rank;
+  for (int i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+  }
+  for (int i = 0; i < rank - 1; ++i) key.strides[i] = strides_bytes[i];
+  for (int e = 0; e < kCache; ++e) {
+    if (cache[e].valid && std::memcmp(&cache[e].key, &key, sizeof(key)) == 0) {
+      *map = cache[e].map;
+      return RD_OK;
+    }
+  }
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return RD_ERR_CUDA;
   cuuint64_t gdim[5], gstride[4];
@@ -96,7 +130,13 @@ rd_status encode(CUtensorMap* map, const void* base, int rank, const uint64_t* d
       fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), gdim, gstride,
          gbox, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? RD_OK : RD_ERR_UNSUPPORTED;
+  if (r != CUDA_SUCCESS) return RD_ERR_UNSUPPORTED;
+  Entry& slot = cache[next_slot];
+  next_slot = (next_slot + 1) % kCache;
+  slot.key = key;
+  slot.map = *map;
+  slot.valid = true;
+  return RD_OK;
 }
 
 // checks shared by the three grouped calls
@@ -138,26 +178,20 @@ int grid_for(int sms, int64_t tiles_upper_bound) {
 // calls, a few rows per expert) the 256-row tile mostly computes padding and
 // single CTAs stream the weights faster.  The choice uses host-known shapes
 // only: pairs when the buffer holds at least 512 rows per group on average.
-// RD_GEMM_VARIANT=single|pair overrides it (for measurements and tests).
+// rd_set_tuning can force either variant.
 bool use_pair(int sms, int64_t m, int32_t g_total) {
   if (sms < 2) return false;
-  const char* v = getenv("RD_GEMM_VARIANT");
-  if (v != nullptr && strcmp(v, "single") == 0) return false;
-  if (v != nullptr && strcmp(v, "pair") == 0) return true;
+  const int32_t v = g_variant.load(std::memory_order_relaxed);
+  if (v == RD_VARIANT_SINGLE) return false;
+  if (v == RD_VARIANT_PAIR) return true;
   return m >= 512 * static_cast<int64_t>(g_total);
 }
 
 // m-tiles per band of the forward / dx tile order: the band's lhs rows stay in
-// L2 while the band sweeps every output column block.  4096 rows by default;
-// RD_BAND_ROWS overrides it (for measurements).
+// L2 while the band sweeps every output column block.
 int32_t band_tiles(bool pair) {
-  int64_t rows = 4096;
-  const char* v = getenv("RD_BAND_ROWS");
-  if (v != nullptr && *v != 0) {
-    char* end = nullptr;
-    const long long r = strtoll(v, &end, 10);
-    if (end != nullptr && *end == 0 && r > 0 && r < (1LL << 30)) rows = r;
-  }
+  const int32_t r = g_band_rows.load(std::memory_order_relaxed);
+  const int64_t rows = r > 0 ? r : kBandRows;
   const int64_t tile = pair ? 2 * kBM : kBM;
   const int64_t t = rows / tile;
   return static_cast<int32_t>(t < 1 ? 1 : t);
@@ -513,6 +547,29 @@ extern "C" rd_status rd_unsort_bwd_rows(const void* g, const void* y, const floa
                                 reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? RD_OK
              : RD_ERR_CUDA;
+}
+
+extern "C" rd_status rd_set_tuning(const rd_tuning* t) {
+  if (t == nullptr) {
+    g_variant.store(RD_VARIANT_AUTO);
+    g_band_rows.store(0);
+    g_timeout_ns.store(0);
+    return RD_OK;
+  }
+  if (t->gemm_variant < RD_VARIANT_AUTO || t->gemm_variant > RD_VARIANT_PAIR || t->band_rows < 0)
+    return RD_ERR_INVALID_ARG;
+  g_variant.store(t->gemm_variant);
+  g_band_rows.store(t->band_rows);
+  g_timeout_ns.store(t->wait_timeout_ns);
+  return RD_OK;
+}
+
+extern "C" rd_status rd_get_tuning(rd_tuning* t) {
+  if (t == nullptr) return RD_ERR_INVALID_ARG;
+  t->gemm_variant = g_variant.load();
+  t->band_rows = g_band_rows.load();
+  t->wait_timeout_ns = g_timeout_ns.load();
+  return RD_OK;
 }
 
 extern "C" const char* rd_status_string(rd_status s) {

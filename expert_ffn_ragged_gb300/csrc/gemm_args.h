@@ -6,13 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-namespace rd {
+#include "schedule.h"
 
-enum GemmOp : int {
-  kOpFwd = 0,  // out[i] = lhs[i] @ rhs[j]             (A K-major, B MN-major)
-  kOpDx = 1,   // out[i] = lhs[i] @ rhs[j]^T           (A K-major, B K-major)
-  kOpDw = 2    // out[j] = x[rows_j]^T @ y[rows_j]     (A MN-major, B MN-major)
-};
+namespace rd {
 
 // What the epilogue does with the f32 accumulator.
 enum GemmEpi : int {
@@ -23,13 +19,15 @@ enum GemmEpi : int {
   kEpiF32Acc = 4   // dw: add the f32 accumulator to the f32 output already in memory
 };
 
-// UMMA tile: 128 x 256 f32 accumulator per CTA, 64-deep K blocks (one
-// 128-byte swizzle atom of bf16).
-constexpr int kBM = 128;
-constexpr int kBN = 256;
-constexpr int kBK = 64;
+// UMMA tile: kBM x kBN (128 x 256) f32 accumulator per CTA, kBK (64) deep K
+// blocks -- one 128-byte swizzle atom of bf16 (schedule.h).
 constexpr int kEpiWarps = 8;    // two epilogue warps per 32-lane quarter of the accumulator
-constexpr int kThreads = 384;   // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue, warp 10 zero fill
+// 12 warps: warp 0 TMA producer, warp 1 MMA issuer, warps 2-9 epilogue (warp % 4
+// is the TMEM lane quarter a warp may read, so warps 2..9 cover each quarter
+// twice), warp 10 zero fill (forward / dx) or dw edge rows.  Warp 11 takes no
+// role: it only joins the block-wide barriers, keeping the block at three
+// whole warpgroups.
+constexpr int kThreads = 384;
 constexpr int kTmemCols = 2 * kBN;  // two accumulators (double buffer)
 constexpr int kMaxGroups = 1024;
 

@@ -48,6 +48,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/rd.h"
 #include "gemm_args.h"
 #include "glu_math.cuh"
@@ -99,16 +101,6 @@ constexpr size_t gemm_smem_bytes_t() {
          sizeof(GemmShared<PAIR>);
 }
 
-// One unit of work as every role sees it.
-struct Tile {
-  int32_t j;         // local group
-  int32_t m_idx;     // row tile (fwd/dx: within the group; dw: within the weight block)
-  int32_t n_idx;     // column tile
-  int32_t rs, re;    // rows of the group, clamped to L
-  int32_t row_load;  // fwd/dx: first row the tile's A rows are loaded from
-  int32_t nkb;       // K blocks (0: the tile is all zeros)
-};
-
 // Exclusive prefix of a per-lane chunk sum across one warp.
 __device__ __forceinline__ long long warp_exclusive_scan(long long v, int lane) {
   long long incl = v;
@@ -142,14 +134,14 @@ __device__ __forceinline__ void build_schedule(GemmShared<PAIR>& sh, const GemmA
   }
   long long run = warp_exclusive_scan(sum, lane);
   for (int i = lo; i < hi; ++i) {
-    sh.bound[i] = static_cast<int32_t>(run < L ? run : L);
+    sh.bound[i] = clamp_boundary(run, L);
     const int s = a.group_sizes[i];
     run += s > 0 ? s : 0;
   }
   const long long total = __shfl_sync(0xFFFFFFFFu, run, 31);
   neg = __any_sync(0xFFFFFFFFu, neg);
   if (lane == 0) {
-    sh.bound[G] = static_cast<int32_t>(total < L ? total : L);
+    sh.bound[G] = clamp_boundary(total, L);
     sh.L = L;
     if (a.status != nullptr && blockIdx.x == 0) {
       int bits = 0;
@@ -164,9 +156,8 @@ __device__ __forceinline__ void build_schedule(GemmShared<PAIR>& sh, const GemmA
   const int per2 = (GL + 31) / 32;
   const int lo2 = min(lane * per2, GL), hi2 = min(lo2 + per2, GL);
   auto tiles_of = [&](int j) -> long long {
-    if (OP == kOpDw) return static_cast<long long>(a.dw_m_tiles) * a.n_tiles;
-    const int cnt = sh.bound[a.group_offset + j + 1] - sh.bound[a.group_offset + j];
-    return static_cast<long long>((cnt + TM - 1) / TM) * a.n_tiles;
+    return tiles_of_group(OP, sh.bound[a.group_offset + j], sh.bound[a.group_offset + j + 1], TM,
+                          a.n_tiles, a.dw_m_tiles);
   };
   long long tsum = 0;
   for (int j = lo2; j < hi2; ++j) tsum += tiles_of(j);
@@ -186,58 +177,16 @@ __device__ __forceinline__ void build_schedule(GemmShared<PAIR>& sh, const GemmA
 
 template <int OP, bool PAIR>
 __device__ __forceinline__ Tile decode_tile(const GemmShared<PAIR>& sh, const GemmArgs& a, int t) {
-  constexpr int TM = TileCfg<PAIR>::kTileM;
-  Tile tl;
-  if (OP == kOpDw) {
-    const int per_group = a.dw_m_tiles * a.n_tiles;
-    tl.j = t / per_group;
-    const int u = t - tl.j * per_group;
-    tl.m_idx = u % a.dw_m_tiles;
-    tl.n_idx = u / a.dw_m_tiles;
-    tl.rs = sh.bound[a.group_offset + tl.j];
-    tl.re = sh.bound[a.group_offset + tl.j + 1];
-    tl.row_load = 0;
-    tl.nkb = (tl.re - tl.rs + kBK - 1) / kBK;
-  } else {
-    int lo = 0, hi = a.g_local;  // tile_start[lo] <= t < tile_start[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (sh.tile_start[mid] <= t) lo = mid; else hi = mid;
-    }
-    tl.j = lo;
-    const int u = t - sh.tile_start[lo];
-    tl.rs = sh.bound[a.group_offset + lo];
-    tl.re = sh.bound[a.group_offset + lo + 1];
-    // Bands of band_tiles m-tiles: within a band the m-tiles run fastest and the
-    // band sweeps every n-tile before the next band starts, so the band's lhs
-    // rows stay in L2 while each rhs column panel is read once per band.
-    const int kBand = a.band_tiles;
-    const int mt = (tl.re - tl.rs + TM - 1) / TM;
-    const int band = u / (kBand * a.n_tiles);
-    const int rem = u - band * kBand * a.n_tiles;
-    const int bw = min(kBand, mt - band * kBand);
-    tl.m_idx = band * kBand + rem % bw;
-    tl.n_idx = rem / bw;
-    const int first = tl.rs + tl.m_idx * TM;
-    tl.row_load = (tl.m_idx == mt - 1) ? tl.re - TM : first;
-    tl.nkb = (a.kc + kBK - 1) / kBK;
-  }
-  return tl;
-}
-
-// dw: rows of the last K block of a group that precede the block's own start
-// (the block is loaded from row end - 64).  Whole 16-row K steps of them are
-// skipped by the MMA; the rows of the step that straddles the start must be
-// zeroed in shared memory.  Returns the first K step to issue and sets
-// [z0, z1) to the rows to zero (empty when z0 == z1).
-__device__ __forceinline__ int dw_edge(const Tile& tl, int kb, int& z0, int& z1) {
-  z0 = z1 = 0;
-  if (kb != tl.nkb - 1) return 0;
-  const int rem = (tl.re - tl.rs) - (tl.nkb - 1) * kBK;
-  const int zrows = kBK - rem;
-  z0 = zrows & ~15;
-  z1 = zrows;
-  return zrows >> 4;
+  SchedView v;
+  v.bound = sh.bound;
+  v.tile_start = sh.tile_start;
+  v.group_offset = a.group_offset;
+  v.g_local = a.g_local;
+  v.n_tiles = a.n_tiles;
+  v.band_tiles = a.band_tiles;
+  v.dw_m_tiles = a.dw_m_tiles;
+  v.kc = a.kc;
+  return decode_tile_view<OP, TileCfg<PAIR>::kTileM>(v, t);
 }
 
 // Zero rows [z0, z1) of one stage of a dw block in both operands: each row is
@@ -360,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t fb = edge ? eb_local : ptx::map_to_rank(fb_local, 0);
             if (edge) ptx::mbar_arrive_expect_tx(eb_local, Cfg::kStageBytes);
             else if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, 2 * Cfg::kStageBytes);
-            const int row0 = (kb == tl.nkb - 1) ? tl.re - kBK : tl.rs + kb * kBK;
+            const int row0 = dw_block_row(tl, kb);
             const int ka = tl.m_idx * TM + static_cast<int>(rank) * kBM;
             const int nb = tl.n_idx * kBN + static_cast<int>(rank) * (kBN / 2);
             // a chunked map lands its 64-column chunks 8 KB apart, as separate boxes would
@@ -412,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               ptx::tma_load_2d(a_dst, &tmap_a, fb, kb * kBK, tl.row_load);
               ptx::tma_load_3d(b_dst, &tmap_b, fb, kb * kBK, tl.n_idx * kBN, tl.j);
             } else {
-              const int row0 = (kb == tl.nkb - 1) ? tl.re - kBK : tl.rs + kb * kBK;
+              const int row0 = dw_block_row(tl, kb);
               if (args.a_chunked) {
                 ptx::tma_load_3d(a_dst, &tmap_a, fb, 0, row0, tl.m_idx * (kBM / 64));
               } else {
@@ -581,8 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // first row of this warp's 32 rows and the rows it may write: [lo, hi)
       const int wrow0 = (OP == kOpDw ? tl.m_idx * TM : tl.row_load) +
                         static_cast<int>(rank) * kBM + q * 32;
-      const int lo = OP == kOpDw ? 0 : tl.rs + tl.m_idx * TM;
-      const int hi = OP == kOpDw ? args.m_out : tl.re;
+      const int lo = OP == kOpDw ? 0 : tile_store_lo(tl, TM);
+      const int hi = OP == kOpDw ? args.m_out : tile_store_hi(tl);
       __nv_bfloat16* base =
           OP == kOpDw ? out + static_cast<size_t>(tl.j) * args.m_out * args.ldo : out;
       const int col0 = tl.n_idx * tile_w;
@@ -822,17 +771,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t lo_bytes = static_cast<uint64_t>(sh.zero_lo) * row_bytes;
       const uint64_t z_bytes = lo_bytes + static_cast<uint64_t>(sh.L - sh.zero_hi) * row_bytes;
       const uint64_t units16 = z_bytes / 16;
-      // weight of a unit: 1, or 2 for the units with one tile fewer (u >= r);
-      // W(u) = total weight of the units before u
-      const int r = total % units;
-      auto W = [&](int u) -> uint64_t {
-        return (r == 0 || u <= r) ? static_cast<uint64_t>(u) : static_cast<uint64_t>(r + 2 * (u - r));
-      };
-      const uint64_t wt = W(units);
-      const uint64_t a0 = units16 * W(unit) / wt, a1 = units16 * W(unit + 1) / wt;
-      const uint64_t per_unit = PAIR ? 2 : 1, sub = PAIR ? (blockIdx.x & 1u) : 0;
-      const uint64_t u0 = a0 + (a1 - a0) * sub / per_unit;
-      const uint64_t u1 = a0 + (a1 - a0) * (sub + 1) / per_unit;
+      uint64_t u0, u1;
+      zero_share(units16, unit, units, total, PAIR, PAIR ? static_cast<int>(blockIdx.x & 1u) : 0,
+                 u0, u1);
       if (u1 > u0) {
         int64_t stages = 0;  // stages this CTA's producer fills in all
         for (int t = unit; t < total; t += units) stages += decode_tile<OP, PAIR>(sh, args, t).nkb;
@@ -894,16 +835,17 @@ template <int OP, int EPI, bool PAIR>
 cudaError_t launch_gemm_impl(const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
                              const GemmArgs& args, int grid, cudaStream_t stream) {
   constexpr size_t smem = gemm_smem_bytes_t<PAIR>();
-  // the shared-memory size attribute is set once per device (it is per-device state)
-  static bool attr_set[64];
+  // the shared-memory size attribute is set once per device (it is per-device
+  // state); two threads racing here both set it, which is harmless
+  static std::atomic<bool> attr_set[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     const cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<OP, EPI, PAIR>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   if (!PAIR) {
     grouped_gemm_kernel<OP, EPI, PAIR><<<grid, kThreads, smem, stream>>>(tmap_a, tmap_b, args);
@@ -923,15 +865,17 @@ cudaError_t launch_gemm_impl(const CUtensorMap& tmap_a, const CUtensorMap& tmap_
   // A persistent grid must not exceed the clusters that can be resident at once:
   // a CTA pair must sit in one GPC, so fewer than (#SMs / 2) pairs may fit.  The
   // limit is queried once per device (it depends only on the kernel and the GPU).
-  static int max_clusters[64];
-  if (max_clusters[dev] == 0) {
+  static std::atomic<int> max_clusters[64];
+  int clusters = max_clusters[dev].load(std::memory_order_acquire);
+  if (clusters == 0) {
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     int n = 0;
     const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<OP, EPI, PAIR>, &cfg);
     if (e != cudaSuccess) return e;
-    max_clusters[dev] = n > 0 ? n : 1;
+    clusters = n > 0 ? n : 1;
+    max_clusters[dev].store(clusters, std::memory_order_release);
   }
-  if (grid > 2 * max_clusters[dev]) grid = 2 * max_clusters[dev];
+  if (grid > 2 * clusters) grid = 2 * clusters;
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<OP, EPI, PAIR>, tmap_a, tmap_b, args);
 }

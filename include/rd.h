@@ -33,11 +33,16 @@
  * *status.  The library never clears *status.
  *
  * Bounded waits: every wait inside the grouped-GEMM kernels gives up after
- * 4 s (or the number of nanoseconds in the environment variable
- * RD_WAIT_TIMEOUT_NS, read at each call).  A kernel that gives up finishes
+ * 4 s (rd_set_tuning can change the bound).  A kernel that gives up finishes
  * its copies and MMAs in flight, frees its tensor memory, returns, and sets
  * RD_STATUS_TIMEOUT; its outputs are then incomplete but the CUDA context
- * stays usable.
+ * stays usable.  Pass a status word to see this: without one a timed-out
+ * call is indistinguishable from a completed one.  An accumulating call
+ * (rd_trans_ragged_dot_f32 with accumulate = 1) that timed out has added
+ * some tiles and not others, so its output buffer is unusable (a retry
+ * would add those tiles twice).
+ *
+ * The library reads no environment variable.
  */
 #ifndef RD_H_
 #define RD_H_
@@ -238,6 +243,46 @@ rd_status rd_glu_bwd(const void* fused, const void* d_out, void* d_fused, int64_
 rd_status rd_unsort_bwd_rows(const void* g, const void* y, const float* w, void* grad, float* dot,
                              int64_t rows, int64_t hidden, const int32_t* limit,
                              rd_stream_t stream);
+
+/*
+ * rd_tuning -- process-wide overrides of the grouped-GEMM launch choices, for
+ * measurements and tests.  No page defines them: they select among kernels
+ * that compute the same result (within the documented accuracy), or bound
+ * the kernels' waits.
+ *
+ *   gemm_variant     RD_VARIANT_AUTO: the library picks the CTA-pair kernel
+ *                    (256-row tiles, cta_group::2) when the buffer holds at
+ *                    least 512 rows per group on average, else the
+ *                    single-CTA kernel (128-row tiles);  RD_VARIANT_SINGLE /
+ *                    RD_VARIANT_PAIR force one of them (all three grouped
+ *                    GEMMs).
+ *   band_rows        rows per band of the forward / dx tile order (within a
+ *                    band the CTAs sweep every output column block before the
+ *                    next band starts, so the band's lhs rows stay in L2);
+ *                    0 = the default, 4096.  Rounded down to whole tiles
+ *                    (at least one).
+ *   wait_timeout_ns  bound of every wait inside the grouped-GEMM kernels;
+ *                    0 = the default, 4 s.
+ *
+ * The values apply to calls made after rd_set_tuning returns, from any
+ * thread; a call reads them on the host when it builds its launch, so a
+ * CUDA graph keeps the values that were in force when it was captured.
+ * rd_set_tuning(NULL) restores the defaults.  Returns RD_ERR_INVALID_ARG
+ * (and changes nothing) for an unknown variant or a negative band_rows.
+ */
+#define RD_VARIANT_AUTO 0
+#define RD_VARIANT_SINGLE 1
+#define RD_VARIANT_PAIR 2
+
+typedef struct {
+  int32_t gemm_variant;
+  int32_t band_rows;
+  uint64_t wait_timeout_ns;
+} rd_tuning;
+
+rd_status rd_set_tuning(const rd_tuning* t);
+/* The values in force (0 fields read back as 0, i.e. the defaults). */
+rd_status rd_get_tuning(rd_tuning* t);
 
 /* A static, human-readable name for a status code. */
 const char* rd_status_string(rd_status s);

@@ -30,8 +30,38 @@ def _declared():
 def test_header_declares_the_abi():
     assert _declared() == sorted([
         "rd_glu_bwd", "rd_glu_fwd", "rd_ragged_dot", "rd_ragged_dot_trans_rhs",
-        "rd_ragged_dot_trans_rhs_glu_bwd", "rd_status_string", "rd_trans_ragged_dot",
-        "rd_trans_ragged_dot_f32", "rd_unsort_bwd_rows"])
+        "rd_get_tuning", "rd_ragged_dot_trans_rhs_glu_bwd", "rd_set_tuning", "rd_status_string",
+        "rd_trans_ragged_dot", "rd_trans_ragged_dot_f32", "rd_unsort_bwd_rows"])
+
+
+class _Tuning(ctypes.Structure):
+    _fields_ = [("gemm_variant", ctypes.c_int32), ("band_rows", ctypes.c_int32),
+                ("wait_timeout_ns", ctypes.c_uint64)]
+
+
+def test_tuning_overrides_on_the_host(lib):
+    """rd_set_tuning / rd_get_tuning need no GPU: set, read back, reject, reset."""
+    lib.rd_set_tuning.restype = lib.rd_get_tuning.restype = ctypes.c_int
+    lib.rd_set_tuning.argtypes = lib.rd_get_tuning.argtypes = [ctypes.c_void_p]
+    t = _Tuning(2, 512, 99)
+    assert lib.rd_set_tuning(ctypes.byref(t)) == RD_OK
+    back = _Tuning()
+    assert lib.rd_get_tuning(ctypes.byref(back)) == RD_OK
+    assert (back.gemm_variant, back.band_rows, back.wait_timeout_ns) == (2, 512, 99)
+    assert lib.rd_set_tuning(ctypes.byref(_Tuning(3, 0, 0))) == RD_ERR_INVALID_ARG
+    assert lib.rd_set_tuning(ctypes.byref(_Tuning(0, -4, 0))) == RD_ERR_INVALID_ARG
+    assert lib.rd_get_tuning(ctypes.byref(back)) == RD_OK and back.band_rows == 512
+    assert lib.rd_get_tuning(None) == RD_ERR_INVALID_ARG
+    assert lib.rd_set_tuning(None) == RD_OK
+    assert lib.rd_get_tuning(ctypes.byref(back)) == RD_OK
+    assert (back.gemm_variant, back.band_rows, back.wait_timeout_ns) == (0, 0, 0)
+
+
+def test_library_reads_no_environment():
+    """No knob of the library hides in an environment variable (all are in rd.h)."""
+    import glob
+    for path in glob.glob(os.path.join(ROOT, "expert_ffn_ragged_gb300", "csrc", "*")):
+        assert "getenv" not in open(path).read(), path
 
 
 def test_every_declared_symbol_is_exported(lib):

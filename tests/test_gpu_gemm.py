@@ -25,10 +25,11 @@ EDGE_SIZES = [0, 1, 127, 128, 129, 0, 255, 3]   # sum 643
 
 
 @pytest.fixture(params=["pair", "single"], autouse=True)
-def gemm_variant(request, monkeypatch):
+def gemm_variant(request, rd_lib):
     """Every test runs on both the CTA-pair (256-row) and the single-CTA (128-row) kernels."""
-    monkeypatch.setenv("RD_GEMM_VARIANT", request.param)
-    return request.param
+    v = rd_lib.VARIANT_PAIR if request.param == "pair" else rd_lib.VARIANT_SINGLE
+    with rd_lib.tuning(variant=v):
+        yield request.param
 
 
 def _normal(rng, shape, var=1.0):
@@ -135,11 +136,13 @@ def run_dw(rd, m, k, n, sizes, off=0, gl=None, limit=None, seed=0):
     if b[off] > 0:
         x_dev[: b[off]] = float("nan")
         y_dev[: b[off]] = float("nan")
-    out = torch.empty((gl, k, n), dtype=torch.bfloat16, device=DEV)
-    out.view(torch.int16).fill_(SENT)
+    buf = torch.empty((gl + 1, k, n), dtype=torch.bfloat16, device=DEV)   # one guard block after
+    buf.view(torch.int16).fill_(SENT)
+    out = buf[:gl]
     rd.trans_ragged_dot(x_dev.to(DEV), y_dev.to(DEV), _i32(sizes), group_offset=off, g_local=gl,
                         limit=None if limit is None else _i32([limit]), out=out)
     torch.cuda.synchronize()
+    assert np.all(obf.torch_bf16_bits(buf[gl]) == SENT), "the guard block after dw was written"
     got = _f64(out)
     x64, y64 = _f64(x), _f64(y)
     ref = oracle.trans_ragged_dot(x64, y64, sizes, off, gl, limit)
@@ -224,6 +227,60 @@ def test_status_bits(rd_lib):
     rd_lib.ragged_dot(lhs, rhs, _i32([100, -5, 200]), status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == (rd_lib.STATUS_NEG_SIZE | rd_lib.STATUS_OVERFLOW)
+
+
+# ------------------------------------------------------------------ tile-order bands
+# The forward / dx tile order walks each group in bands of band_tiles m-tiles
+# (the last band of a group partial), sweeping every column block inside a
+# band.  With the default 4096-row band only groups above 4096 rows span
+# several bands, so these tests shrink the band to 1, 2 and 3 tiles: groups of
+# 600 to 2000 rows then hold up to 16 bands, most of them with a partial last
+# band, over several column tiles, and every output element is compared.
+BAND_SIZES = [1500, 0, 700, 2000, 613, 1, 1100]     # sum 5914
+
+
+@pytest.mark.parametrize("band_tiles", [1, 2, 3])
+def test_band_order_forward(rd_lib, gemm_variant, band_tiles):
+    tile = 256 if gemm_variant == "pair" else 128
+    with rd_lib.tuning(band_rows=band_tiles * tile):
+        run_fwd(rd_lib, 6000, 64, 776, BAND_SIZES, seed=band_tiles)
+        run_fwd(rd_lib, 6000, 64, 776, BAND_SIZES, off=2, gl=4, limit=5000, seed=band_tiles + 10)
+
+
+@pytest.mark.parametrize("band_tiles", [1, 3])
+def test_band_order_forward_glu(rd_lib, gemm_variant, band_tiles):
+    tile = 256 if gemm_variant == "pair" else 128
+    with rd_lib.tuning(band_rows=band_tiles * tile):
+        run_fwd(rd_lib, 6000, 64, 1040, BAND_SIZES, glu=True, seed=band_tiles + 20)
+
+
+@pytest.mark.parametrize("band_tiles", [1, 2, 3])
+def test_band_order_dx(rd_lib, gemm_variant, band_tiles):
+    tile = 256 if gemm_variant == "pair" else 128
+    with rd_lib.tuning(band_rows=band_tiles * tile):
+        run_dx(rd_lib, 6000, 776, 64, BAND_SIZES, seed=band_tiles + 30)
+        run_dx(rd_lib, 6000, 520, 64, BAND_SIZES, off=1, gl=5, limit=4500, seed=band_tiles + 40)
+
+
+@pytest.mark.parametrize("band_tiles", [1, 3])
+def test_band_order_dx_glu_bwd(rd_lib, gemm_variant, band_tiles):
+    tile = 256 if gemm_variant == "pair" else 128
+    with rd_lib.tuning(band_rows=band_tiles * tile):
+        run_dx_glu_bwd(rd_lib, 6000, 520, 64, BAND_SIZES, limit=5500, seed=band_tiles + 50)
+
+
+def test_tuning_round_trip(rd_lib):
+    """rd_set_tuning / rd_get_tuning: values read back, bad ones rejected, defaults restored."""
+    before = rd_lib.get_tuning()
+    with rd_lib.tuning(band_rows=768, wait_timeout_ns=123456789):
+        t = rd_lib.get_tuning()
+        assert t["band_rows"] == 768 and t["wait_timeout_ns"] == 123456789
+        with pytest.raises(rd_lib.RdError):
+            rd_lib.set_tuning(variant=7)
+        with pytest.raises(rd_lib.RdError):
+            rd_lib.set_tuning(band_rows=-1)
+        assert rd_lib.get_tuning()["band_rows"] == 768
+    assert rd_lib.get_tuning() == before
 
 
 # ------------------------------------------------------------------ dx
@@ -362,11 +419,17 @@ def run_dw_f32(rd, m, k, n, sizes, off=0, gl=None, limit=None, seed=0, accumulat
         x_dev[: b[off]] = float("nan")
         y_dev[: b[off]] = float("nan")
     prior = torch.from_numpy(rng.standard_normal((gl, k, n)).astype(np.float32))
-    out = prior.clone().to(DEV) if accumulate else torch.full((gl, k, n), float("nan"), device=DEV)
+    buf = torch.full((gl + 1, k, n), 5.5, device=DEV)          # one guard block after the output
+    out = buf[:gl]
+    if accumulate:
+        out.copy_(prior.to(DEV))
+    else:
+        out.fill_(float("nan"))
     rd.trans_ragged_dot_f32(x_dev.to(DEV), y_dev.to(DEV), _i32(sizes), group_offset=off, g_local=gl,
                             limit=None if limit is None else _i32([limit]), out=out,
                             accumulate=accumulate)
     torch.cuda.synchronize()
+    assert bool((buf[gl] == 5.5).all()), "the guard block after dw was written"
     got = out.cpu().numpy().astype(np.float64)
     x64, y64 = _f64(x), _f64(y)
     p64 = prior.numpy().astype(np.float64)

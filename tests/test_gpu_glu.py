@@ -16,6 +16,7 @@ pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
 SENT = 0x3C3C
+CANARY_ROWS = 4     # rows after each output buffer that no call may touch
 SPECIAL = np.array([0x0000, 0x8000, 0x7F80, 0xFF80, 0x7FC0, 0x0001, 0x8001, 0x007F, 0x3F80,
                     0xBF80], np.uint16)
 
@@ -62,13 +63,13 @@ def test_glu_fwd_exhaustive_gates(rd_lib, rows, f, limit):
     fused_dev = _bits_tensor(fused).to(DEV)
     if L < rows:
         fused_dev[L:] = float("nan")
-    out = torch.empty((rows, f), dtype=torch.bfloat16, device=DEV)
-    out.view(torch.int16).fill_(SENT)
+    buf = torch.empty((rows + CANARY_ROWS, f), dtype=torch.bfloat16, device=DEV)
+    buf.view(torch.int16).fill_(SENT)
     rd_lib.glu_fwd(fused_dev, limit=None if limit is None else torch.tensor([limit], dtype=torch.int32,
-                                                                             device=DEV), out=out)
+                                                                             device=DEV), out=buf[:rows])
     torch.cuda.synchronize()
-    got = obf.torch_bf16_bits(out)
-    assert np.all(got[L:] == SENT)
+    got = obf.torch_bf16_bits(buf)
+    assert np.all(got[L:] == SENT), "a row past the limit or a canary row after the output was written"
     g = obf.bits_to_f32(fused[:L, :f])
     u = obf.bits_to_f32(fused[:L, f:])
     ref64 = oracle.glu_fwd_f64(g, u)
@@ -85,13 +86,13 @@ def test_glu_bwd_exhaustive_gates(rd_lib, rows, f, limit):
     if L < rows:
         fused_dev[L:] = float("nan")
         d_dev[L:] = float("nan")
-    out = torch.empty((rows, 2 * f), dtype=torch.bfloat16, device=DEV)
-    out.view(torch.int16).fill_(SENT)
+    buf = torch.empty((rows + CANARY_ROWS, 2 * f), dtype=torch.bfloat16, device=DEV)
+    buf.view(torch.int16).fill_(SENT)
     rd_lib.glu_bwd(fused_dev, d_dev, limit=None if limit is None else torch.tensor([limit], dtype=torch.int32,
-                                                                                     device=DEV), out=out)
+                                                                                     device=DEV), out=buf[:rows])
     torch.cuda.synchronize()
-    got = obf.torch_bf16_bits(out)
-    assert np.all(got[L:] == SENT)
+    got = obf.torch_bf16_bits(buf)
+    assert np.all(got[L:] == SENT), "a row past the limit or a canary row after the output was written"
     g = obf.bits_to_f32(fused[:L, :f])
     u = obf.bits_to_f32(fused[:L, f:])
     dd = obf.bits_to_f32(d[:L])
@@ -104,24 +105,37 @@ def test_glu_bwd_exhaustive_gates(rd_lib, rows, f, limit):
 
 @pytest.mark.parametrize("limit", [0, 1, 1023, 125952, 126156, 225280])
 def test_glu_limits_packed_buffer_rows(rd_lib, limit):
-    """The page's limit list on a [225280, 2*256] buffer: rows >= limit untouched."""
+    """The page's limit list on a [225280, 2*256] buffer: rows >= limit untouched.
+
+    Every valid row of both outputs is compared with the oracle (forward and
+    backward, each against its float64 value and the f32 op sequence's special
+    bits), and canary rows after both buffers must keep their sentinel.
+    """
     rows, f = 225280, 256
     gen = torch.Generator(device=DEV).manual_seed(limit + 1)
     fused = torch.randn((rows, 2 * f), generator=gen, device=DEV).to(torch.bfloat16)
-    out = torch.empty((rows, f), dtype=torch.bfloat16, device=DEV)
-    out.view(torch.int16).fill_(SENT)
+    obuf = torch.empty((rows + CANARY_ROWS, f), dtype=torch.bfloat16, device=DEV)
+    obuf.view(torch.int16).fill_(SENT)
+    out = obuf[:rows]
     lim = torch.tensor([limit], dtype=torch.int32, device=DEV)
     rd_lib.glu_fwd(fused, limit=lim, out=out)
-    dout = torch.empty((rows, 2 * f), dtype=torch.bfloat16, device=DEV)
-    dout.view(torch.int16).fill_(SENT)
-    rd_lib.glu_bwd(fused, out, limit=lim, out=dout)
+    dbuf = torch.empty((rows + CANARY_ROWS, 2 * f), dtype=torch.bfloat16, device=DEV)
+    dbuf.view(torch.int16).fill_(SENT)
+    rd_lib.glu_bwd(fused, out, limit=lim, out=dbuf[:rows])
     torch.cuda.synchronize()
     sent = torch.tensor(SENT, dtype=torch.int16, device=DEV)
-    assert bool((out[limit:].view(torch.int16) == sent).all())
-    assert bool((dout[limit:].view(torch.int16) == sent).all())
-    if limit:
-        rows_s = np.unique(np.r_[0, limit - 1, np.random.default_rng(limit).integers(0, limit, 64)])
-        fb = obf.torch_bf16_bits(fused[rows_s])
+    assert bool((obuf[limit:].view(torch.int16) == sent).all())
+    assert bool((dbuf[limit:].view(torch.int16) == sent).all())
+    for r0 in range(0, limit, 32768):
+        r1 = min(r0 + 32768, limit)
+        fb = obf.torch_bf16_bits(fused[r0:r1])
         g, u = obf.bits_to_f32(fb[:, :f]), obf.bits_to_f32(fb[:, f:])
         bits, _ = oracle.glu_fwd_f32(g, u)
-        _compare(obf.torch_bf16_bits(out[rows_s]), g, oracle.glu_fwd_f64(g, u), bits, "glu_fwd rows")
+        got = obf.torch_bf16_bits(out[r0:r1])
+        _compare(got, g, oracle.glu_fwd_f64(g, u), bits, f"glu_fwd rows [{r0}, {r1})")
+        dd = obf.bits_to_f32(got)        # the backward's d is the forward's output
+        want_g64, want_u64 = oracle.glu_bwd_f64(g, u, dd)
+        (bg, bu), _ = oracle.glu_bwd_f32(g, u, dd)
+        gotd = obf.torch_bf16_bits(dbuf[r0:r1])
+        _compare(gotd[:, :f], g, want_g64, bg, f"glu_bwd d_gate rows [{r0}, {r1})")
+        _compare(gotd[:, f:], g, want_u64, bu, f"glu_bwd d_up rows [{r0}, {r1})")

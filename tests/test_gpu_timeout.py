@@ -1,7 +1,7 @@
 """Failure detection on the GPU without a fault: every bounded wait runs out.
 
-With RD_WAIT_TIMEOUT_NS=1 each wait inside the grouped-GEMM kernel gives up at
-once.  The kernel must then unwind (let its copies and MMAs in flight finish,
+With the wait bound set to 1 ns (rd_set_tuning) each wait inside the
+grouped-GEMM kernel gives up at once.  The kernel must then unwind (let its copies and MMAs in flight finish,
 free its tensor memory), return, and report RD_STATUS_TIMEOUT through the
 status word; the next call on the same context must be correct again.
 """
@@ -45,19 +45,19 @@ def _call(rd, op, a, w, do, gs, status):
 
 @pytest.mark.parametrize("variant,op", [("single", "fwd"), ("pair", "fwd"), ("single", "dx"),
                                         ("pair", "dx"), ("single", "dw"), ("pair", "dw")])
-def test_timeout_unwinds_and_reports(rd_lib, monkeypatch, variant, op):
-    monkeypatch.setenv("RD_GEMM_VARIANT", variant)
+def test_timeout_unwinds_and_reports(rd_lib, variant, op):
+    v = rd_lib.VARIANT_PAIR if variant == "pair" else rd_lib.VARIANT_SINGLE
     a, w, do, sizes = _inputs(op, 1)
     gs = torch.tensor(sizes, dtype=torch.int32, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    monkeypatch.setenv("RD_WAIT_TIMEOUT_NS", "1")
-    _call(rd_lib, op, a, w, do, gs, status)
+    with rd_lib.tuning(variant=v, wait_timeout_ns=1):
+        _call(rd_lib, op, a, w, do, gs, status)
     torch.cuda.synchronize()
     assert int(status.item()) & rd_lib.STATUS_TIMEOUT
     # the context, the tensor memory and the library are usable again
-    monkeypatch.delenv("RD_WAIT_TIMEOUT_NS")
     status.zero_()
-    out = _call(rd_lib, op, a, w, do, gs, status)
+    with rd_lib.tuning(variant=v):
+        out = _call(rd_lib, op, a, w, do, gs, status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     a64, w64, d64 = obf.torch_bf16_to_f64(a), obf.torch_bf16_to_f64(w), obf.torch_bf16_to_f64(do)

@@ -17,6 +17,7 @@ pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
 SENT = 0x3C3C
+CANARY_ROWS = 4     # rows after each output buffer that no call may touch
 
 
 def _run(rd, rows, hidden, limit, seed):
@@ -30,15 +31,17 @@ def _run(rd, rows, hidden, limit, seed):
     gd[L:] = float("nan")
     yd[L:] = float("nan")
     wd[L:] = float("nan")
-    grad = torch.empty_like(gd)
-    grad.view(torch.int16).fill_(SENT)
-    dot = torch.full((rows,), 7.0, dtype=torch.float32, device=DEV)
+    gbuf = torch.empty((rows + CANARY_ROWS, hidden), dtype=torch.bfloat16, device=DEV)
+    gbuf.view(torch.int16).fill_(SENT)
+    dbuf = torch.full((rows + CANARY_ROWS,), 7.0, dtype=torch.float32, device=DEV)
+    grad, dot = gbuf[:rows], dbuf[:rows]
     rd.unsort_bwd_rows(gd, yd, wd, limit=None if limit is None else torch.tensor([limit], dtype=torch.int32, device=DEV),
                        grad=grad, dot=dot)
     torch.cuda.synchronize()
-    gb = obf.torch_bf16_bits(grad)
-    assert np.all(gb[L:] == SENT), "gradient rows past the limit were written"
-    assert bool((dot[L:] == 7.0).all()), "dot entries past the limit were written"
+    gb = obf.torch_bf16_bits(gbuf)
+    assert np.all(gb[L:] == SENT), "gradient rows past the limit (or canary rows) were written"
+    assert bool((dbuf[L:] == 7.0).all()), "dot entries past the limit (or canaries) were written"
+    gb = gb[:rows]
     g32, y32 = g.float().numpy(), y.float().numpy()
     bits, _, ref = unsort.unsort_bwd_rows(g32, y32, w.numpy(), limit)
     np.testing.assert_array_equal(gb[:L], bits)
@@ -54,22 +57,24 @@ def test_unsort_bwd_rows(rd_lib, hidden, limit):
 
 
 def test_unsort_bwd_rows_packed_buffer(rd_lib):
-    """The page's bench shape: [225280, 4096] with 126156 valid rows (sampled rows checked)."""
+    """The page's bench shape: [225280, 4096] with 126156 valid rows, every valid row checked."""
     rows, hidden, limit = 225280, 4096, 126156
     gen = torch.Generator(device=DEV).manual_seed(7)
     g = torch.randn((rows, hidden), generator=gen, device=DEV).to(torch.bfloat16)
     y = torch.randn((rows, hidden), generator=gen, device=DEV).to(torch.bfloat16)
     w = torch.rand((rows,), generator=gen, device=DEV) * 2 - 1
-    grad = torch.empty_like(g)
-    grad.view(torch.int16).fill_(SENT)
-    dot = torch.full((rows,), 7.0, dtype=torch.float32, device=DEV)
+    gbuf = torch.empty((rows + CANARY_ROWS, hidden), dtype=torch.bfloat16, device=DEV)
+    gbuf.view(torch.int16).fill_(SENT)
+    dbuf = torch.full((rows + CANARY_ROWS,), 7.0, dtype=torch.float32, device=DEV)
+    grad, dot = gbuf[:rows], dbuf[:rows]
     rd_lib.unsort_bwd_rows(g, y, w, limit=torch.tensor([limit], dtype=torch.int32, device=DEV), grad=grad, dot=dot)
     torch.cuda.synchronize()
-    assert bool((grad[limit:].view(torch.int16) == SENT).all())
-    assert bool((dot[limit:] == 7.0).all())
-    rs = torch.from_numpy(np.unique(np.r_[0, limit - 1, np.random.default_rng(1).integers(0, limit, 96)])).to(DEV)
-    g32, y32 = g[rs].float().cpu().numpy(), y[rs].float().cpu().numpy()
-    bits, _, ref = unsort.unsort_bwd_rows(g32, y32, w[rs].cpu().numpy())
-    np.testing.assert_array_equal(obf.torch_bf16_bits(grad[rs]), bits)
-    err = np.abs(dot[rs].cpu().numpy().astype(np.float64) - ref)
-    assert np.all(err <= unsort.dot_tolerance(g32, y32))
+    assert bool((gbuf[limit:].view(torch.int16) == SENT).all())
+    assert bool((dbuf[limit:] == 7.0).all())
+    for r0 in range(0, limit, 16384):
+        r1 = min(r0 + 16384, limit)
+        g32, y32 = g[r0:r1].float().cpu().numpy(), y[r0:r1].float().cpu().numpy()
+        bits, _, ref = unsort.unsort_bwd_rows(g32, y32, w[r0:r1].cpu().numpy())
+        np.testing.assert_array_equal(obf.torch_bf16_bits(grad[r0:r1]), bits)
+        err = np.abs(dot[r0:r1].cpu().numpy().astype(np.float64) - ref)
+        assert np.all(err <= unsort.dot_tolerance(g32, y32)), f"row dot rows [{r0}, {r1})"
