@@ -53,7 +53,7 @@ _lib = None
 
 class _Tuning(ctypes.Structure):
     _fields_ = [("gemm_variant", ctypes.c_int32), ("band_rows", ctypes.c_int32),
-                ("wait_timeout_ns", ctypes.c_uint64)]
+                ("wait_timeout_ns", ctypes.c_uint64), ("reserved", ctypes.c_int32 * 2)]
 
 
 class RdError(RuntimeError):

@@ -556,7 +556,8 @@ extern "C" rd_status rd_set_tuning(const rd_tuning* t) {
     g_timeout_ns.store(0);
     return RD_OK;
   }
-  if (t->gemm_variant < RD_VARIANT_AUTO || t->gemm_variant > RD_VARIANT_PAIR || t->band_rows < 0)
+  if (t->gemm_variant < RD_VARIANT_AUTO || t->gemm_variant > RD_VARIANT_PAIR ||
+      t->band_rows < 0 || t->reserved[0] != 0 || t->reserved[1] != 0)
     return RD_ERR_INVALID_ARG;
   g_variant.store(t->gemm_variant);
   g_band_rows.store(t->band_rows);
@@ -569,6 +570,7 @@ extern "C" rd_status rd_get_tuning(rd_tuning* t) {
   t->gemm_variant = g_variant.load();
   t->band_rows = g_band_rows.load();
   t->wait_timeout_ns = g_timeout_ns.load();
+  t->reserved[0] = t->reserved[1] = 0;
   return RD_OK;
 }
 

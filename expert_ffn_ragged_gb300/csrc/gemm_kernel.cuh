@@ -208,6 +208,73 @@ __device__ __forceinline__ void dw_zero_rows(uint8_t* a_st, uint8_t* b_st, int z
   ptx::fence_proxy_async_smem();
 }
 
+// One TMA box of a ring stage: which tensor map (A or B), its coordinates
+// (innermost first) and where it lands inside the stage's A or B tile.
+struct Box {
+  int32_t x, y, z;
+  uint32_t off;  // bytes from the start of the stage's A (or B) tile
+  bool on;       // this slot carries a box
+  bool b;        // tensor map B (else A)
+  bool d3;       // 3-D map (else 2-D)
+};
+
+// The boxes that fill one ring stage of this CTA: K block kb of tile tl.
+// Slots are fixed per configuration (compile-time indices keep the list in
+// registers); unused slots have on == false.
+template <int OP, bool PAIR, bool GLU>
+__device__ __forceinline__ void stage_boxes(const Tile& tl, int kb, uint32_t rank, const GemmArgs& a,
+                                            Box (&bx)[6]) {
+  constexpr int TM = TileCfg<PAIR>::kTileM;
+  constexpr uint32_t kChunk = kBK * 128;  // bytes of one 64-wide chunk of a stage tile
+  auto put = [&](int i, bool on, bool b, bool d3, int32_t x, int32_t y, int32_t z, uint32_t off) {
+    bx[i].x = x;
+    bx[i].y = y;
+    bx[i].z = z;
+    bx[i].off = off;
+    bx[i].on = on;
+    bx[i].b = b;
+    bx[i].d3 = d3;
+  };
+#pragma unroll
+  for (int i = 0; i < 6; ++i) bx[i].on = false;
+  if (OP == kOpDw) {
+    // a chunked map lands its 64-column chunks 8 KB apart, as separate boxes would
+    const int row0 = dw_block_row(tl, kb);
+    const int ka = tl.m_idx * TM + static_cast<int>(rank) * kBM;
+    constexpr int b_cols = PAIR ? kBN / 2 : kBN;
+    const int nb = tl.n_idx * kBN + static_cast<int>(rank) * b_cols;
+    const bool ac = a.a_chunked != 0, bc = a.b_chunked != 0;
+    put(0, true, false, ac, ac ? 0 : ka, row0, ac ? ka / 64 : 0, 0);
+    put(1, !ac, false, false, ka + 64, row0, 0, kChunk);
+    put(2, true, true, bc, bc ? 0 : nb, row0, bc ? nb / 64 : 0, 0);
+#pragma unroll
+    for (int c = 1; c < b_cols / 64; ++c) put(2 + c, !bc, true, false, nb + c * 64, row0, 0, c * kChunk);
+    return;
+  }
+  const int arow = tl.row_load + static_cast<int>(rank) * kBM;
+  put(0, true, false, false, kb * kBK, arow, 0, 0);
+  if (OP == kOpFwd) {
+    // rhs [g, k, n] as (n, k, g): MN-major B, 64 columns per box
+    constexpr int kBoxes = PAIR ? 2 : 4;
+#pragma unroll
+    for (int c = 0; c < kBoxes; ++c) {
+      int x;
+      if (GLU) {
+        // gate columns then up columns (in a pair: the even CTA gate, the odd CTA up)
+        const bool up = PAIR ? rank != 0 : c >= 2;
+        x = (up ? a.glu_f : 0) + tl.n_idx * (kBN / 2) + (PAIR ? c : (c & 1)) * 64;
+      } else {
+        x = tl.n_idx * kBN + static_cast<int>(rank) * (kBN / 2) + c * 64;
+      }
+      put(1 + c, true, true, true, x, kb * kBK, tl.j, c * kChunk);
+    }
+  } else {
+    // dx: w [g, k, n] as (n, k, g): the K-major B of w^T, one box
+    put(1, true, true, true, kb * kBK, tl.n_idx * kBN + static_cast<int>(rank) * (PAIR ? kBN / 2 : 0),
+        tl.j, 0);
+  }
+}
+
 template <int OP, int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
@@ -305,77 +372,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             edge = z1 > z0;
           }
           const uint32_t eb_local = ptx::smem_addr(&sh.efull[stage]);
-          if (PAIR && OP == kOpDw) {
-            const uint32_t fb = edge ? eb_local : ptx::map_to_rank(fb_local, 0);
+          uint32_t fb;
+          if (PAIR) {
+            // Non-edge fills of both CTAs count on the even CTA's barrier, which expects
+            // them all; the odd CTA's copies may land before that expectation is posted
+            // (the phase cannot complete before the even CTA's arrival).
+            fb = edge ? eb_local : ptx::map_to_rank(fb_local, 0);
             if (edge) ptx::mbar_arrive_expect_tx(eb_local, Cfg::kStageBytes);
             else if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, 2 * Cfg::kStageBytes);
-            const int row0 = dw_block_row(tl, kb);
-            const int ka = tl.m_idx * TM + static_cast<int>(rank) * kBM;
-            const int nb = tl.n_idx * kBN + static_cast<int>(rank) * (kBN / 2);
-            // a chunked map lands its 64-column chunks 8 KB apart, as separate boxes would
-            if (args.a_chunked) {
-              ptx::tma_load_3d_pair(a_dst, &tmap_a, fb, 0, row0, ka / 64);
-            } else {
-#pragma unroll
-              for (int c = 0; c < 2; ++c)
-                ptx::tma_load_2d_pair(a_dst + c * (kBK * 128), &tmap_a, fb, ka + c * 64, row0);
-            }
-            if (args.b_chunked) {
-              ptx::tma_load_3d_pair(b_dst, &tmap_b, fb, 0, row0, nb / 64);
-            } else {
-#pragma unroll
-              for (int c = 0; c < 2; ++c)
-                ptx::tma_load_2d_pair(b_dst + c * (kBK * 128), &tmap_b, fb, nb + c * 64, row0);
-            }
-          } else if (PAIR) {
-            // Both CTAs' bytes are counted on the even CTA's barrier, which expects them
-            // all; the odd CTA's copies may land before that expectation is posted (the
-            // phase cannot complete before the even CTA's arrival).
-            const uint32_t fb = ptx::map_to_rank(fb_local, 0);
-            if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, 2 * Cfg::kStageBytes);
-            const int arow = tl.row_load + static_cast<int>(rank) * kBM;
-            ptx::tma_load_2d_pair(a_dst, &tmap_a, fb, kb * kBK, arow);
-            if (OP == kOpFwd) {
-#pragma unroll
-              for (int c = 0; c < 2; ++c) {
-                const int x = GLU ? ((rank == 0 ? 0 : args.glu_f) + tl.n_idx * (kBN / 2) + c * 64)
-                                  : (tl.n_idx * kBN + static_cast<int>(rank) * (kBN / 2) + c * 64);
-                ptx::tma_load_3d_pair(b_dst + c * (kBK * 128), &tmap_b, fb, x, kb * kBK, tl.j);
-              }
-            } else {
-              ptx::tma_load_3d_pair(b_dst, &tmap_b, fb, kb * kBK,
-                                    tl.n_idx * kBN + static_cast<int>(rank) * (kBN / 2), tl.j);
-            }
           } else {
-            const uint32_t fb = edge ? eb_local : fb_local;
+            fb = edge ? eb_local : fb_local;
             ptx::mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
-            if (OP == kOpFwd) {
-              ptx::tma_load_2d(a_dst, &tmap_a, fb, kb * kBK, tl.row_load);
+          }
+          Box bx[6];
+          stage_boxes<OP, PAIR, GLU>(tl, kb, rank, args, bx);
 #pragma unroll
-              for (int c = 0; c < 4; ++c) {
-                const int x = GLU ? ((c < 2 ? 0 : args.glu_f) + tl.n_idx * (kBN / 2) + (c & 1) * 64)
-                                  : (tl.n_idx * kBN + c * 64);
-                ptx::tma_load_3d(b_dst + c * (kBK * 128), &tmap_b, fb, x, kb * kBK, tl.j);
-              }
-            } else if (OP == kOpDx) {
-              ptx::tma_load_2d(a_dst, &tmap_a, fb, kb * kBK, tl.row_load);
-              ptx::tma_load_3d(b_dst, &tmap_b, fb, kb * kBK, tl.n_idx * kBN, tl.j);
+          for (int i = 0; i < 6; ++i) {
+            if (!bx[i].on) continue;
+            const uint32_t dst = (bx[i].b ? b_dst : a_dst) + bx[i].off;
+            const CUtensorMap* map = bx[i].b ? &tmap_b : &tmap_a;
+            if (PAIR) {
+              if (bx[i].d3) ptx::tma_load_3d_pair(dst, map, fb, bx[i].x, bx[i].y, bx[i].z);
+              else ptx::tma_load_2d_pair(dst, map, fb, bx[i].x, bx[i].y);
             } else {
-              const int row0 = dw_block_row(tl, kb);
-              if (args.a_chunked) {
-                ptx::tma_load_3d(a_dst, &tmap_a, fb, 0, row0, tl.m_idx * (kBM / 64));
-              } else {
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-                  ptx::tma_load_2d(a_dst + c * (kBK * 128), &tmap_a, fb, tl.m_idx * kBM + c * 64, row0);
-              }
-              if (args.b_chunked) {
-                ptx::tma_load_3d(b_dst, &tmap_b, fb, 0, row0, tl.n_idx * (kBN / 64));
-              } else {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                  ptx::tma_load_2d(b_dst + c * (kBK * 128), &tmap_b, fb, tl.n_idx * kBN + c * 64, row0);
-              }
+              if (bx[i].d3) ptx::tma_load_3d(dst, map, fb, bx[i].x, bx[i].y, bx[i].z);
+              else ptx::tma_load_2d(dst, map, fb, bx[i].x, bx[i].y);
             }
           }
           pend_mask |= 1u << stage;

@@ -263,12 +263,14 @@ rd_status rd_unsort_bwd_rows(const void* g, const void* y, const float* w, void*
  *                    (at least one).
  *   wait_timeout_ns  bound of every wait inside the grouped-GEMM kernels;
  *                    0 = the default, 4 s.
+ *   reserved         must be 0 (room for later fields).
  *
  * The values apply to calls made after rd_set_tuning returns, from any
  * thread; a call reads them on the host when it builds its launch, so a
  * CUDA graph keeps the values that were in force when it was captured.
  * rd_set_tuning(NULL) restores the defaults.  Returns RD_ERR_INVALID_ARG
- * (and changes nothing) for an unknown variant or a negative band_rows.
+ * (and changes nothing) for an unknown variant, a negative band_rows or a
+ * nonzero reserved field.
  */
 #define RD_VARIANT_AUTO 0
 #define RD_VARIANT_SINGLE 1
@@ -278,6 +280,7 @@ typedef struct {
   int32_t gemm_variant;
   int32_t band_rows;
   uint64_t wait_timeout_ns;
+  int32_t reserved[2];
 } rd_tuning;
 
 rd_status rd_set_tuning(const rd_tuning* t);

@@ -36,7 +36,7 @@ def test_header_declares_the_abi():
 
 class _Tuning(ctypes.Structure):
     _fields_ = [("gemm_variant", ctypes.c_int32), ("band_rows", ctypes.c_int32),
-                ("wait_timeout_ns", ctypes.c_uint64)]
+                ("wait_timeout_ns", ctypes.c_uint64), ("reserved", ctypes.c_int32 * 2)]
 
 
 def test_tuning_overrides_on_the_host(lib):
@@ -50,6 +50,9 @@ def test_tuning_overrides_on_the_host(lib):
     assert (back.gemm_variant, back.band_rows, back.wait_timeout_ns) == (2, 512, 99)
     assert lib.rd_set_tuning(ctypes.byref(_Tuning(3, 0, 0))) == RD_ERR_INVALID_ARG
     assert lib.rd_set_tuning(ctypes.byref(_Tuning(0, -4, 0))) == RD_ERR_INVALID_ARG
+    bad = _Tuning(0, 0, 0)
+    bad.reserved[1] = 1
+    assert lib.rd_set_tuning(ctypes.byref(bad)) == RD_ERR_INVALID_ARG
     assert lib.rd_get_tuning(ctypes.byref(back)) == RD_OK and back.band_rows == 512
     assert lib.rd_get_tuning(None) == RD_ERR_INVALID_ARG
     assert lib.rd_set_tuning(None) == RD_OK
