@@ -354,7 +354,9 @@ def run_ops(rd, device, stream, peaks):
         res["dx"] = {"us": t * 1e6, "tflops": F / t / 1e12,
                      "bound": "hbm" if B / BW > F / P else "tensor",
                      "frac": max(F / P, B / BW) / t}
-        t = med(lambda: rd.trans_ragged_dot(x, do, gs, out=dw), entry="dw")
+        # dw through per-group tensor maps, in a workspace allocated once
+        ws = torch.empty(rd.dw_workspace_bytes(device), dtype=torch.uint8, device=device)
+        t = med(lambda: rd.trans_ragged_dot(x, do, gs, out=dw, workspace=ws), entry="dw")
         B = w.m * w.k * 2 + w.m * w.n * 2 + w.g_total * w.k * w.n * 2
         res["dw"] = {"us": t * 1e6, "tflops": F / t / 1e12,
                      "bound": "hbm" if B / BW > F / P else "tensor",
@@ -364,7 +366,8 @@ def run_ops(rd, device, stream, peaks):
         # dw kept in f32 (stored, then added into an existing gradient buffer)
         dw32 = torch.zeros((w.g_total, w.k, w.n), dtype=torch.float32, device=device)
         for key, acc in (("dw_f32", False), ("dw_f32_accumulate", True)):
-            t = med(lambda: rd.trans_ragged_dot_f32(x, do, gs, out=dw32, accumulate=acc), entry=key)
+            t = med(lambda: rd.trans_ragged_dot_f32(x, do, gs, out=dw32, accumulate=acc, workspace=ws),
+                    entry=key)
             # storing writes every block (empty groups' as zeros); accumulating reads
             # and writes only the blocks of groups with rows
             B = w.m * w.k * 2 + w.m * w.n * 2 + (live * w.k * w.n * 4 * 2 if acc
@@ -372,7 +375,7 @@ def run_ops(rd, device, stream, peaks):
             res[key] = {"us": t * 1e6, "tflops": F / t / 1e12,
                         "bound": "tensor" if F / P >= B / BW else "hbm",
                         "frac": max(F / P, B / BW) / t}
-        del x, do, wt, dw32
+        del x, do, wt, dw32, ws
         torch.cuda.empty_cache()
 
         # decode pair (up with GLU, down) sharing group_sizes inside one CUDA graph
@@ -822,12 +825,13 @@ def run_profile(args):
         fn = lambda: rd.ragged_dot(lhs, rhs, gs, w.group_offset, lim, rd.EPI_SILU_GLU, out)
     elif name in ("dx", "dw", "dw_f32acc"):
         w = workloads.backward_pair()
+        ws = torch.empty(rd.dw_workspace_bytes(device), dtype=torch.uint8, device=device)
         gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=device)
         do = normal_bf16((w.m, w.n), 1.0, 41, device)
         if name == "dw_f32acc":
             x = normal_bf16((w.m, w.k), 1.0, 40, device)
             dw32 = torch.zeros((w.g_total, w.k, w.n), dtype=torch.float32, device=device)
-            fn = lambda: rd.trans_ragged_dot_f32(x, do, gs, out=dw32, accumulate=True)
+            fn = lambda: rd.trans_ragged_dot_f32(x, do, gs, out=dw32, accumulate=True, workspace=ws)
         elif name == "dx":
             wt = normal_bf16((w.g_total, w.k, w.n), w.rhs_var, 42, device)
             dx = torch.empty((w.m, w.k), dtype=torch.bfloat16, device=device)
@@ -835,7 +839,7 @@ def run_profile(args):
         else:
             x = normal_bf16((w.m, w.k), 1.0, 40, device)
             dw = torch.empty((w.g_total, w.k, w.n), dtype=torch.bfloat16, device=device)
-            fn = lambda: rd.trans_ragged_dot(x, do, gs, out=dw)
+            fn = lambda: rd.trans_ragged_dot(x, do, gs, out=dw, workspace=ws)
     elif name == "packed_dx_glu_bwd":
         w = workloads.packed_glu_fwd()
         gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=device)

@@ -12,6 +12,7 @@ Functions (same names as the C ABI, without the ``rd_`` prefix):
 * ``ragged_dot_trans_rhs_glu_bwd(d_out, rhs, fused, group_sizes, ...)`` -> [d_gate | d_up] [m, 2f]
 * ``trans_ragged_dot(x, y, group_sizes, ...)``           -> out [g_local, k, n]
 * ``trans_ragged_dot_f32(x, y, group_sizes, ..., accumulate=False)`` -> f32 out [g_local, k, n]
+* ``dw_workspace_bytes(device)``                         -> the dw calls' workspace size
 * ``glu_fwd(fused, limit=None)``                         -> out [rows, f]
 * ``glu_bwd(fused, d_out, limit=None)``                  -> d_fused [rows, 2f]
 * ``unsort_bwd_rows(g, y, w, limit=None)``                -> (grad [rows, hidden], dot [rows])
@@ -30,7 +31,7 @@ from typing import Optional
 
 __all__ = [
     "load", "lib_path", "ragged_dot", "ragged_dot_trans_rhs", "ragged_dot_trans_rhs_glu_bwd",
-    "trans_ragged_dot", "trans_ragged_dot_f32",
+    "trans_ragged_dot", "trans_ragged_dot_f32", "dw_workspace_bytes",
     "glu_fwd", "glu_bwd", "unsort_bwd_rows", "RdError", "EPI_NONE", "EPI_SILU_GLU",
     "STATUS_NEG_SIZE", "STATUS_OVERFLOW", "STATUS_TIMEOUT", "MAX_GROUPS",
     "VARIANT_AUTO", "VARIANT_SINGLE", "VARIANT_PAIR", "set_tuning", "get_tuning", "tuning",
@@ -81,8 +82,11 @@ def load():
     lib.rd_ragged_dot.argtypes = grouped + [ctypes.c_int, ip, vp]
     lib.rd_ragged_dot_trans_rhs.argtypes = grouped + [ip, vp]
     lib.rd_ragged_dot_trans_rhs_glu_bwd.argtypes = [vp] + grouped + [ip, vp]
-    lib.rd_trans_ragged_dot.argtypes = grouped + [ip, vp]
-    lib.rd_trans_ragged_dot_f32.argtypes = grouped + [i32, ip, vp]
+    sz = ctypes.c_size_t
+    lib.rd_trans_ragged_dot.argtypes = grouped + [vp, sz, ip, vp]
+    lib.rd_trans_ragged_dot_f32.argtypes = grouped + [i32, vp, sz, ip, vp]
+    lib.rd_trans_ragged_dot_workspace_size.argtypes = [ctypes.c_void_p]
+    lib.rd_trans_ragged_dot_workspace_size.restype = ctypes.c_int
     lib.rd_glu_fwd.argtypes = [vp, vp, i64, i64, ip, vp]
     lib.rd_glu_bwd.argtypes = [vp, vp, vp, i64, i64, ip, vp]
     lib.rd_unsort_bwd_rows.argtypes = [vp, vp, vp, vp, vp, i64, i64, ip, vp]
@@ -326,6 +330,42 @@ def ragged_dot_trans_rhs_glu_bwd(d_out, rhs, fused, group_sizes, group_offset: i
     return out
 
 
+_ws_bytes = {}
+
+
+def dw_workspace_bytes(device=None) -> int:
+    """Bytes of the dw workspace (rd_trans_ragged_dot_workspace_size) on a CUDA device."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if dev.index not in _ws_bytes:
+        lib = load()
+        n = ctypes.c_size_t(0)
+        with _on_device(dev):
+            _check(lib.rd_trans_ragged_dot_workspace_size(ctypes.byref(n)),
+                   "rd_trans_ragged_dot_workspace_size")
+        _ws_bytes[dev.index] = n.value
+    return _ws_bytes[dev.index]
+
+
+def _dw_workspace(workspace, dev, stream):
+    """The workspace argument of the dw calls: "auto" allocates one for this call."""
+    import torch
+
+    if workspace is None:
+        return None
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError('workspace must be "auto", None or a uint8 CUDA tensor')
+        ws = torch.empty(dw_workspace_bytes(dev), dtype=torch.uint8, device=dev)
+        if stream is not None and stream != torch.cuda.current_stream(dev):
+            ws.record_stream(stream)     # freed after the call: keep it until the stream is done
+        return ws
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous uint8 CUDA tensor")
+    return workspace
+
+
 def _dw_args(x, y, group_sizes, group_offset, g_local, limit, status):
     _bf16_2d(x, "x")
     _bf16_2d(y, "y")
@@ -340,8 +380,12 @@ def _dw_args(x, y, group_sizes, group_offset, g_local, limit, status):
 
 
 def trans_ragged_dot(x, y, group_sizes, group_offset: int = 0, g_local: Optional[int] = None,
-                     limit=None, out=None, status=None, stream=None):
-    """out[j] = x[rows_j]^T @ y[rows_j] for the local groups; x [m, k], y [m, n]."""
+                     limit=None, out=None, status=None, stream=None, workspace="auto"):
+    """out[j] = x[rows_j]^T @ y[rows_j] for the local groups; x [m, k], y [m, n].
+
+    workspace: "auto" (a workspace of dw_workspace_bytes() allocated for the
+    call), None (the form without one), or a caller's uint8 CUDA tensor.
+    """
     import torch
 
     lib = load()
@@ -350,17 +394,20 @@ def trans_ragged_dot(x, y, group_sizes, group_offset: int = 0, g_local: Optional
     if out is None:
         out = torch.empty((g_local, k, n), dtype=torch.bfloat16, device=dev)
     _out(out, (g_local, k, n), torch.bfloat16)
-    _same_device(dev, y, out, group_sizes, limit, status)
+    ws = _dw_workspace(workspace, dev, stream)
+    _same_device(dev, y, out, group_sizes, limit, status, ws)
     with _on_device(dev):
         code = lib.rd_trans_ragged_dot(_ptr(x), _ptr(y), _ptr(out), m, k, n, _ptr(group_sizes),
                                        group_sizes.numel(), group_offset, g_local, _ptr(limit),
-                                       _ptr(status), _stream(stream, dev))
+                                       _ptr(ws), 0 if ws is None else ws.numel(), _ptr(status),
+                                       _stream(stream, dev))
     _check(code, "rd_trans_ragged_dot")
     return out
 
 
 def trans_ragged_dot_f32(x, y, group_sizes, group_offset: int = 0, g_local: Optional[int] = None,
-                         limit=None, out=None, accumulate: bool = False, status=None, stream=None):
+                         limit=None, out=None, accumulate: bool = False, status=None, stream=None,
+                         workspace="auto"):
     """out[j] (+)= x[rows_j]^T @ y[rows_j] in f32; ``accumulate`` adds into ``out``.
 
     An accumulating call whose status reports STATUS_TIMEOUT has added some
@@ -376,11 +423,13 @@ def trans_ragged_dot_f32(x, y, group_sizes, group_offset: int = 0, g_local: Opti
             raise ValueError("accumulate needs an existing out buffer")
         out = torch.empty((g_local, k, n), dtype=torch.float32, device=dev)
     _out(out, (g_local, k, n), torch.float32)
-    _same_device(dev, y, out, group_sizes, limit, status)
+    ws = _dw_workspace(workspace, dev, stream)
+    _same_device(dev, y, out, group_sizes, limit, status, ws)
     with _on_device(dev):
         code = lib.rd_trans_ragged_dot_f32(_ptr(x), _ptr(y), _ptr(out), m, k, n,
                                            _ptr(group_sizes), group_sizes.numel(), group_offset,
                                            g_local, _ptr(limit), 1 if accumulate else 0,
+                                           _ptr(ws), 0 if ws is None else ws.numel(),
                                            _ptr(status), _stream(stream, dev))
     _check(code, "rd_trans_ragged_dot_f32")
     return out

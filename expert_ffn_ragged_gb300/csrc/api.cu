@@ -368,10 +368,13 @@ namespace {
 rd_status trans_ragged_impl(const void* x, const void* y, void* out, int64_t m, int64_t k,
                             int64_t n, const int32_t* group_sizes, int32_t g_total,
                             int32_t group_offset, int32_t g_local, const int32_t* limit,
-                            int epi, int32_t* status, rd_stream_t stream) {
+                            int epi, void* workspace, size_t workspace_bytes, int32_t* status,
+                            rd_stream_t stream) {
   const uint64_t out_elem = epi == kEpiNone ? 2 : 4;
   rd_status st = check_groups(m, k, n, group_sizes, g_total, group_offset, g_local, limit, status);
   if (st != RD_OK) return st;
+  if (workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 127u))
+    return RD_ERR_UNSUPPORTED;
   if ((m > 0 && k > 0 && x == nullptr) || (m > 0 && n > 0 && y == nullptr) ||
       (k > 0 && n > 0 && out == nullptr))
     return RD_ERR_INVALID_ARG;
@@ -382,6 +385,16 @@ rd_status trans_ragged_impl(const void* x, const void* y, void* out, int64_t m, 
     return RD_ERR_INVALID_ARG;
   int sms = 0;
   if ((st = current_device(&sms)) != RD_OK) return st;
+  // the workspace holds the per-group maps of every CTA; it must not overlap
+  // anything the call reads or writes
+  const uint64_t ws_need = static_cast<uint64_t>(sms) * kMapBytesPerCta;
+  if (workspace != nullptr &&
+      (workspace_bytes < ws_need ||
+       out_aliases(workspace, workspace_bytes, x, static_cast<uint64_t>(m) * k * 2, y,
+                   static_cast<uint64_t>(m) * n * 2, group_sizes,
+                   static_cast<uint64_t>(g_total) * 4, limit, status) ||
+       overlap(workspace, workspace_bytes, out, static_cast<uint64_t>(g_local) * k * n * out_elem)))
+    return RD_ERR_INVALID_ARG;
   if (k == 0 || n == 0) return RD_OK;
 
   const bool pair = use_pair(sms, m, g_total);
@@ -435,6 +448,15 @@ rd_status trans_ragged_impl(const void* x, const void* y, void* out, int64_t m, 
   a.g_local = g_local;
   a.n_tiles = static_cast<int32_t>((n + kBN - 1) / kBN);
   a.dw_m_tiles = static_cast<int32_t>((k + tile_rows - 1) / tile_rows);
+  // with a workspace each CTA rebases the maps to each group it works on (rows
+  // outside the group then arrive as zeros); without one the edge rows of each
+  // group's first block are zeroed in shared memory
+  a.group_maps = workspace != nullptr ? 1 : 0;
+  a.x_base = x;
+  a.y_base = y;
+  a.x_row_bytes = k * 2;
+  a.y_row_bytes = n * 2;
+  a.maps = static_cast<CUtensorMap*>(workspace);
   a.timeout_ns = wait_timeout_ns();
   const int64_t tiles = static_cast<int64_t>(g_local) * a.dw_m_tiles * a.n_tiles;
   if (tiles > kMaxDim) return RD_ERR_UNSUPPORTED;
@@ -449,21 +471,33 @@ rd_status trans_ragged_impl(const void* x, const void* y, void* out, int64_t m, 
 extern "C" rd_status rd_trans_ragged_dot(const void* x, const void* y, void* out, int64_t m,
                                          int64_t k, int64_t n, const int32_t* group_sizes,
                                          int32_t g_total, int32_t group_offset, int32_t g_local,
-                                         const int32_t* limit, int32_t* status,
+                                         const int32_t* limit, void* workspace,
+                                         size_t workspace_bytes, int32_t* status,
                                          rd_stream_t stream) {
   return trans_ragged_impl(x, y, out, m, k, n, group_sizes, g_total, group_offset, g_local, limit,
-                           kEpiNone, status, stream);
+                           kEpiNone, workspace, workspace_bytes, status, stream);
+}
+
+extern "C" rd_status rd_trans_ragged_dot_workspace_size(size_t* bytes) {
+  if (bytes == nullptr) return RD_ERR_INVALID_ARG;
+  int sms = 0;
+  const rd_status st = current_device(&sms);
+  if (st != RD_OK) return st;
+  *bytes = static_cast<size_t>(sms) * kMapBytesPerCta;
+  return RD_OK;
 }
 
 extern "C" rd_status rd_trans_ragged_dot_f32(const void* x, const void* y, float* out, int64_t m,
                                              int64_t k, int64_t n, const int32_t* group_sizes,
                                              int32_t g_total, int32_t group_offset,
                                              int32_t g_local, const int32_t* limit,
-                                             int32_t accumulate, int32_t* status,
+                                             int32_t accumulate, void* workspace,
+                                             size_t workspace_bytes, int32_t* status,
                                              rd_stream_t stream) {
   if (accumulate != 0 && accumulate != 1) return RD_ERR_INVALID_ARG;
   return trans_ragged_impl(x, y, out, m, k, n, group_sizes, g_total, group_offset, g_local, limit,
-                           accumulate ? kEpiF32Acc : kEpiF32, status, stream);
+                           accumulate ? kEpiF32Acc : kEpiF32, workspace, workspace_bytes, status,
+                           stream);
 }
 
 namespace {

@@ -52,8 +52,23 @@ struct GemmArgs {
   int32_t band_tiles;          // fwd/dx: m-tiles per band of the tile order (lhs rows kept in L2)
   int32_t a_chunked;           // dw: tmap_a is (64, rows, width / 64): one box per stage
   int32_t b_chunked;           // dw: tmap_b likewise (else 2-D maps, one box per 64 columns)
+  // dw with per-group tensor maps (group_maps != 0): the CTA builds the maps of
+  // its tiles' groups from tmap_a / tmap_b into its slots of `maps` (kMapSlots
+  // pairs a CTA, global memory), rebasing them to each group's first row
+  int32_t group_maps;
+  const void* x_base;          // dw: x (the A operand) and y (the B operand)
+  const void* y_base;
+  int64_t x_row_bytes;
+  int64_t y_row_bytes;
+  CUtensorMap* maps;           // [grid][kMapSlots][2]
   uint64_t timeout_ns;         // bound of every wait inside the kernel
 };
+
+// Per-group tensor-map slots of one CTA (a ring: slot i % kMapSlots serves the
+// CTA's i-th tile with rows).  It is longer than the operand ring, so a slot
+// is rewritten only after every copy through its previous maps has landed.
+constexpr int kMapSlots = 8;
+constexpr size_t kMapBytesPerCta = static_cast<size_t>(kMapSlots) * 2 * 128;
 
 // `pair`: the CTA-pair variant (clusters of two CTAs, 256-row tiles); `grid`
 // must then be even.

@@ -73,8 +73,9 @@ struct TileCfg {
 };
 
 template <bool PAIR>
-struct alignas(16) GemmShared {
+struct alignas(128) GemmShared {
   static constexpr int S = TileCfg<PAIR>::kStagesN;
+  uint8_t mapstage[2][128];  // dw with group maps: the two maps being rebased (128-byte aligned)
   uint64_t full[S];
   uint64_t empty[S];
   uint64_t efull[S];   // dw: this CTA's copy of an edge block landed (edge fills only)
@@ -89,8 +90,9 @@ struct alignas(16) GemmShared {
   int32_t zero_lo;  // forward/dx: rows [0, zero_lo) are zero
   int32_t zero_hi;  // forward/dx: rows [zero_hi, L) are zero
   int32_t fills;      // stages the producer has filled so far (paces the zero fill)
+  int32_t maps_built;  // dw with group maps: tiles with rows whose maps are published
   int32_t bound[kMaxGroups + 1];       // group boundaries, clamped to L
-  int32_t tile_start[kMaxGroups + 1];  // first tile of each local group
+  int32_t tile_start[kMaxGroups + 1];  // fwd/dx: first tile of each local group; dw: group order
   uint4 epi[kEpiWarps][32 * 4];        // epilogue staging per warp: 32 rows x 64 bytes
   uint4 zeros[256];                    // 4 KB zero block, the source of the zero-fill copies
 };
@@ -159,16 +161,33 @@ __device__ __forceinline__ void build_schedule(GemmShared<PAIR>& sh, const GemmA
     return tiles_of_group(OP, sh.bound[a.group_offset + j], sh.bound[a.group_offset + j + 1], TM,
                           a.n_tiles, a.dw_m_tiles);
   };
+  if (OP == kOpDw) {
+    // the tile order's group sequence: groups without rows first, each part in
+    // index order (a warp partition: empties before this lane's chunk, and after)
+    int n_empty = 0;
+    for (int j = lo2; j < hi2; ++j) n_empty += group_is_empty(sh.bound, a.group_offset, j) ? 1 : 0;
+    const int e_before = static_cast<int>(warp_exclusive_scan(n_empty, lane));
+    const int e_total = __shfl_sync(0xFFFFFFFFu, e_before + n_empty, 31);
+    int pe = e_before, pn = e_total + (lo2 - e_before);
+    for (int j = lo2; j < hi2; ++j) {
+      if (group_is_empty(sh.bound, a.group_offset, j)) sh.tile_start[pe++] = j;
+      else sh.tile_start[pn++] = j;
+    }
+  }
   long long tsum = 0;
   for (int j = lo2; j < hi2; ++j) tsum += tiles_of(j);
   long long trun = warp_exclusive_scan(tsum, lane);
-  for (int j = lo2; j < hi2; ++j) {
-    sh.tile_start[j] = static_cast<int32_t>(trun);
-    trun += tiles_of(j);
+  if (OP != kOpDw) {
+    for (int j = lo2; j < hi2; ++j) {
+      sh.tile_start[j] = static_cast<int32_t>(trun);
+      trun += tiles_of(j);
+    }
+  } else {
+    trun += tsum;
   }
   const long long ttotal = __shfl_sync(0xFFFFFFFFu, trun, 31);
   if (lane == 0) {
-    sh.tile_start[GL] = static_cast<int32_t>(ttotal);
+    if (OP != kOpDw) sh.tile_start[GL] = static_cast<int32_t>(ttotal);
     sh.total_tiles = static_cast<int32_t>(ttotal);
     sh.zero_lo = sh.bound[a.group_offset];
     sh.zero_hi = sh.bound[a.group_offset + GL];
@@ -208,6 +227,24 @@ __device__ __forceinline__ void dw_zero_rows(uint8_t* a_st, uint8_t* b_st, int z
   ptx::fence_proxy_async_smem();
 }
 
+// Wait until *counter > value: a bounded poll on a shared-memory counter that
+// another warp of the CTA advances (gives up like mbar_wait_bounded).
+__device__ __forceinline__ bool wait_counter_above(const volatile int32_t* counter, int32_t value,
+                                                   volatile int* abort_flag, uint64_t limit_ns) {
+  if (*counter > value) return true;
+  const uint64_t t0 = ptx::global_timer_ns();
+#pragma unroll 1
+  while (*counter <= value) {
+    if (*abort_flag) return false;
+    if (ptx::global_timer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
 // One TMA box of a ring stage: which tensor map (A or B), its coordinates
 // (innermost first) and where it lands inside the stage's A or B tile.
 struct Box {
@@ -238,8 +275,11 @@ __device__ __forceinline__ void stage_boxes(const Tile& tl, int kb, uint32_t ran
 #pragma unroll
   for (int i = 0; i < 6; ++i) bx[i].on = false;
   if (OP == kOpDw) {
-    // a chunked map lands its 64-column chunks 8 KB apart, as separate boxes would
-    const int row0 = dw_block_row(tl, kb);
+    // a chunked map lands its 64-column chunks 8 KB apart, as separate boxes would;
+    // with group maps the rows are counted from the group's first row
+    int row0;
+    if (a.group_maps) dw_group_block(tl, kb, &row0);
+    else row0 = dw_block_row(tl, kb);
     const int ka = tl.m_idx * TM + static_cast<int>(rank) * kBM;
     constexpr int b_cols = PAIR ? kBN / 2 : kBN;
     const int nb = tl.n_idx * kBN + static_cast<int>(rank) * b_cols;
@@ -315,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(ptx::smem_addr(&sh.drain), 1);
     sh.abort_flag = 0;
     sh.fills = 0;
+    sh.maps_built = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0 && lane == 0 && args.kc > 0) {
@@ -349,15 +390,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t fpar = 0, epar = 0;            // per-slot parities of full / efull
       int32_t n_fills = 0;
       bool ok = true;
+      int32_t map_tiles = 0;  // dw with group maps: tiles with rows so far
       for (int t = unit; t < total && ok; t += units) {
         const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
-        for (int kb = 0; kb < tl.nkb; ++kb) {
-          if (!ptx::mbar_wait_bounded(ptx::smem_addr(&sh.empty[stage]), phase ^ 1,
-                                              abort_flag, tlimit)) {
+        const CUtensorMap* map_a = &tmap_a;
+        const CUtensorMap* map_b = &tmap_b;
+        if (OP == kOpDw && args.group_maps && tl.nkb > 0) {
+          // this tile's maps (rebased to its group by the map warp): wait until they
+          // are published, then acquire them for the copies
+          if (!wait_counter_above(&sh.maps_built, map_tiles, abort_flag, tlimit)) {
             ok = false;
             break;
           }
-          pend_mask &= ~(1u << stage);
+          map_a = args.maps + (static_cast<size_t>(blockIdx.x) * kMapSlots + map_tiles % kMapSlots) * 2;
+          map_b = map_a + 1;
+          ptx::tmap_acquire(map_a);
+          ptx::tmap_acquire(map_b);
+          ++map_tiles;
+        }
+        for (int kb = 0; kb < tl.nkb; ++kb) {
+          // Everything this fill needs is worked out before waiting for its slot, so
+          // that the copies go out as soon as the slot is free (with the operands
+          // arriving just in time, any work between the two adds to every block).
           const uint32_t fb_local = ptx::smem_addr(&sh.full[stage]);
           const uint32_t a_dst = ptx::smem_addr(sA + stage * Cfg::kStageA);
           const uint32_t b_dst = ptx::smem_addr(sB + stage * Cfg::kStageB);
@@ -366,31 +420,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           // own edge barrier (efull), which only edge blocks use; the edge warp waits
           // there, zeroes, and signals the MMA.
           bool edge = false;
-          if (OP == kOpDw) {
+          if (OP == kOpDw && !args.group_maps) {
             int z0, z1;
             dw_edge(tl, kb, z0, z1);
             edge = z1 > z0;
           }
           const uint32_t eb_local = ptx::smem_addr(&sh.efull[stage]);
-          uint32_t fb;
-          if (PAIR) {
-            // Non-edge fills of both CTAs count on the even CTA's barrier, which expects
-            // them all; the odd CTA's copies may land before that expectation is posted
-            // (the phase cannot complete before the even CTA's arrival).
-            fb = edge ? eb_local : ptx::map_to_rank(fb_local, 0);
-            if (edge) ptx::mbar_arrive_expect_tx(eb_local, Cfg::kStageBytes);
-            else if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, 2 * Cfg::kStageBytes);
-          } else {
-            fb = edge ? eb_local : fb_local;
-            ptx::mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
-          }
+          // Non-edge fills of both CTAs of a pair count on the even CTA's barrier, which
+          // expects them all; the odd CTA's copies may land before that expectation is
+          // posted (the phase cannot complete before the even CTA's arrival).
+          const uint32_t fb = edge ? eb_local : (PAIR ? ptx::map_to_rank(fb_local, 0) : fb_local);
           Box bx[6];
           stage_boxes<OP, PAIR, GLU>(tl, kb, rank, args, bx);
+          if (!ptx::mbar_wait_bounded(ptx::smem_addr(&sh.empty[stage]), phase ^ 1,
+                                              abort_flag, tlimit)) {
+            ok = false;
+            break;
+          }
+          pend_mask &= ~(1u << stage);
+          if (!PAIR || edge) ptx::mbar_arrive_expect_tx(fb, Cfg::kStageBytes);
+          else if (rank == 0) ptx::mbar_arrive_expect_tx(fb_local, 2 * Cfg::kStageBytes);
 #pragma unroll
           for (int i = 0; i < 6; ++i) {
             if (!bx[i].on) continue;
             const uint32_t dst = (bx[i].b ? b_dst : a_dst) + bx[i].off;
-            const CUtensorMap* map = bx[i].b ? &tmap_b : &tmap_a;
+            const CUtensorMap* map = bx[i].b ? map_b : map_a;
             if (PAIR) {
               if (bx[i].d3) ptx::tma_load_3d_pair(dst, map, fb, bx[i].x, bx[i].y, bx[i].z);
               else ptx::tma_load_2d_pair(dst, map, fb, bx[i].x, bx[i].y);
@@ -466,9 +520,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           int kk0 = 0;  // first 16-deep K step issued for this block
           bool edge = false;
           if (OP == kOpDw) {
-            int z0, z1;
-            kk0 = dw_edge(tl, kb, z0, z1);
-            edge = z1 > z0;
+            if (args.group_maps) {
+              // the first block's rows above the group arrived as zeros: skip their
+              // whole 16-row steps
+              int row;
+              kk0 = dw_group_block(tl, kb, &row);
+            } else {
+              int z0, z1;
+              kk0 = dw_edge(tl, kb, z0, z1);
+              edge = z1 > z0;
+            }
+          }
+          // the block's operand descriptors, worked out before its wait (as the
+          // producer does for its copies) so that the MMAs issue as soon as it lands
+          const uint32_t a_addr = ptx::smem_addr(sA + stage * Cfg::kStageA);
+          const uint32_t b_addr = ptx::smem_addr(sB + stage * Cfg::kStageB);
+          auto a_desc = [&](int kk) {
+            return a_mn ? ptx::sw128_desc(a_addr + kk * 2048, kBK * 128, 1024)
+                        : ptx::sw128_desc(a_addr + kk * 32, 16, 1024);
+          };
+          auto b_desc = [&](int kk) {
+            return b_mn ? ptx::sw128_desc(b_addr + kk * 2048, b_lbo, 1024)
+                        : ptx::sw128_desc(b_addr + kk * 32, 16, 1024);
+          };
+          uint64_t ad[kBK / 16], bd[kBK / 16];
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            ad[kk] = a_desc(kk);
+            bd[kk] = b_desc(kk);
           }
           if (edge) {
             // rows of a neighbouring group (or a NaN) must not enter the sum: the
@@ -486,14 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           ptx::tc_fence_after();
-          const uint32_t a_addr = ptx::smem_addr(sA + stage * Cfg::kStageA);
-          const uint32_t b_addr = ptx::smem_addr(sB + stage * Cfg::kStageB);
-          // one 16-deep K step of the block into the accumulator
-          auto mma_step = [&](int kk, uint32_t accum) {
-            const uint64_t adesc = a_mn ? ptx::sw128_desc(a_addr + kk * 2048, kBK * 128, 1024)
-                                        : ptx::sw128_desc(a_addr + kk * 32, 16, 1024);
-            const uint64_t bdesc = b_mn ? ptx::sw128_desc(b_addr + kk * 2048, b_lbo, 1024)
-                                        : ptx::sw128_desc(b_addr + kk * 32, 16, 1024);
+          auto mma = [&](uint64_t adesc, uint64_t bdesc, uint32_t accum) {
             if (PAIR) ptx::tc_mma_bf16_pair(d_tmem, adesc, bdesc, idesc, accum);
             else ptx::tc_mma_bf16(d_tmem, adesc, bdesc, idesc, accum);
           };
@@ -501,10 +573,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // every block but a dw group's straddling last one: four MMAs back to
             // back (with a skip test in front of each, dw's issue took ~1.3x as long)
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) mma_step(kk, (kb > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk) mma(ad[kk], bd[kk], (kb > 0 || kk > 0) ? 1u : 0u);
           } else {
 #pragma unroll 1
-            for (int kk = kk0; kk < kBK / 16; ++kk) mma_step(kk, (kb > 0 || kk > kk0) ? 1u : 0u);
+            for (int kk = kk0; kk < kBK / 16; ++kk)
+              mma(a_desc(kk), b_desc(kk), (kb > 0 || kk > kk0) ? 1u : 0u);
           }
           if (PAIR) ptx::tc_commit_pair(ptx::smem_addr(&sh.empty[stage]), 0x3);
           else ptx::tc_commit(ptx::smem_addr(&sh.empty[stage]));
@@ -738,6 +811,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
+    }
+  } else if (OP == kOpDw && warp == 2 + kEpiWarps && args.group_maps) {
+    // ------------------------------------------------------------ dw group maps
+    // For each of this CTA's tiles with rows, rebase copies of the x and y maps to
+    // the tile's group (address = the group's first row, rows = the group's rows)
+    // and publish them to the CTA's next map slot, ahead of the producer.  Rows
+    // outside the group are then out of bounds for the copies and land as zeros,
+    // so no block needs zeroing.  A slot is rewritten only once the producer has
+    // filled a whole ring beyond the last block read through it, i.e. once every
+    // copy through its previous maps has landed.
+    const uint32_t st_a = ptx::smem_addr(sh.mapstage[0]);
+    const uint32_t st_b = ptx::smem_addr(sh.mapstage[1]);
+    const uint4* src_a = reinterpret_cast<const uint4*>(&tmap_a);
+    const uint4* src_b = reinterpret_cast<const uint4*>(&tmap_b);
+    int64_t fills_end[kMapSlots];  // per slot: producer fills through its last tile
+    int64_t fills = 0;
+    int32_t built = 0;
+    bool ok = true;
+    for (int t = unit; t < total && ok; t += units) {
+      const Tile tl = decode_tile<OP, PAIR>(sh, args, t);
+      fills += tl.nkb;
+      if (tl.nkb == 0) continue;
+      const int slot = built % kMapSlots;
+      if (built >= kMapSlots) {
+        ok = wait_counter_above(&sh.fills, static_cast<int32_t>(fills_end[slot] + S - 1), abort_flag,
+                                tlimit);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        if (!ok) break;
+      }
+      if (lane < 8) reinterpret_cast<uint4*>(sh.mapstage[0])[lane] = src_a[lane];
+      else if (lane < 16) reinterpret_cast<uint4*>(sh.mapstage[1])[lane - 8] = src_b[lane - 8];
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t rows = static_cast<uint32_t>(tl.re - tl.rs);
+        ptx::tmap_replace_address(st_a, static_cast<const char*>(args.x_base) +
+                                            static_cast<int64_t>(tl.rs) * args.x_row_bytes);
+        ptx::tmap_replace_dim1(st_a, rows);
+        ptx::tmap_replace_address(st_b, static_cast<const char*>(args.y_base) +
+                                            static_cast<int64_t>(tl.rs) * args.y_row_bytes);
+        ptx::tmap_replace_dim1(st_b, rows);
+      }
+      __syncwarp();
+      CUtensorMap* dst = args.maps + (static_cast<size_t>(blockIdx.x) * kMapSlots + slot) * 2;
+      ptx::tmap_publish(dst, st_a);
+      ptx::tmap_publish(dst + 1, st_b);
+      fills_end[slot] = fills;
+      ++built;
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        *reinterpret_cast<volatile int32_t*>(&sh.maps_built) = built;
+      }
     }
   } else if (OP == kOpDw && warp == 2 + kEpiWarps) {
     // ------------------------------------------------------------ dw edge rows

@@ -304,6 +304,38 @@ __device__ __forceinline__ void tmem_load_32cols(uint32_t taddr, uint32_t (&r)[3
       : "memory");
 }
 
+// ------------------------------------------------- tensor maps built on the device
+// A tensor map (128 bytes) staged in shared memory is edited field by field,
+// then copied to global memory with a release of the tensor-map proxy; a
+// thread that then issues copies through the global copy first acquires it.
+__device__ __forceinline__ void tmap_replace_address(uint32_t smem_map, const void* addr) {
+  asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(smem_map),
+               "l"(reinterpret_cast<uint64_t>(addr))
+               : "memory");
+}
+
+// the extent of dimension 1 (the rows of the maps this library builds)
+__device__ __forceinline__ void tmap_replace_dim1(uint32_t smem_map, uint32_t extent) {
+  asm volatile("tensormap.replace.tile.global_dim.shared::cta.b1024.b32 [%0], 1, %1;" ::"r"(smem_map),
+               "r"(extent)
+               : "memory");
+}
+
+// warp-wide: copy the 128-byte map at smem_map to global_map (64-byte aligned)
+__device__ __forceinline__ void tmap_publish(void* global_map, uint32_t smem_map) {
+  asm volatile(
+      "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned"
+      " [%0], [%1], 128;" ::"l"(reinterpret_cast<uint64_t>(global_map)),
+      "r"(smem_map)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmap_acquire(const void* global_map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
+                   reinterpret_cast<uint64_t>(global_map))
+               : "memory");
+}
+
 // ------------------------------------------------- UMMA operand descriptors
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile:
 //   bits  0-13 start address >> 4

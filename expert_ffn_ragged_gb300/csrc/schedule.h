@@ -54,7 +54,9 @@ struct Tile {
 // The schedule's inputs: the boundary and tile-prefix arrays plus the sizes.
 struct SchedView {
   const int32_t* bound;       // [g_total + 1] group boundaries, clamped to L
-  const int32_t* tile_start;  // [g_local + 1] first tile of each local group
+  const int32_t* tile_start;  // fwd/dx: [g_local + 1] first tile of each local group;
+                              // dw: [g_local] the local group at each position of the
+                              // tile order (groups without rows first)
   int32_t group_offset;
   int32_t g_local;
   int32_t n_tiles;
@@ -62,6 +64,13 @@ struct SchedView {
   int32_t dw_m_tiles;   // dw
   int32_t kc;           // fwd/dx contraction length
 };
+
+// dw visits the groups without rows first: their tiles only write zeros (no
+// MMA), so handing them out at the start lets those writes overlap the first
+// real tiles and leaves the real tiles evenly spread over the CTAs.
+RD_HD bool group_is_empty(const int32_t* bound, int group_offset, int j) {
+  return bound[group_offset + j + 1] == bound[group_offset + j];
+}
 
 RD_HD int32_t clamp_boundary(long long run, int32_t L) {
   return static_cast<int32_t>(run < L ? run : L);
@@ -80,8 +89,9 @@ RD_HD Tile decode_tile_view(const SchedView& v, int t) {
   Tile tl;
   if (OP == kOpDw) {
     const int per_group = v.dw_m_tiles * v.n_tiles;
-    tl.j = t / per_group;
-    const int u = t - tl.j * per_group;
+    const int pos = t / per_group;
+    tl.j = v.tile_start[pos];
+    const int u = t - pos * per_group;
     tl.m_idx = u % v.dw_m_tiles;
     tl.n_idx = u / v.dw_m_tiles;
     tl.rs = v.bound[v.group_offset + tl.j];
@@ -139,6 +149,19 @@ RD_HD int dw_edge(const Tile& tl, int kb, int& z0, int& z1) {
   z0 = zrows & ~15;
   z1 = zrows;
   return zrows >> 4;
+}
+
+// dw through per-group tensor maps (the map's rows are the group's rows, so
+// rows outside the group are out of bounds and land as zeros): the K blocks
+// are aligned to end at the group end, block kb starting at group row
+// rem - 64 + 64 kb with rem = the rows of the last block (1..64); the first
+// block's rows above the group start arrive as zeros, and its whole 16-row
+// steps of them are skipped.  Returns the first K step to issue; *row
+// receives the block's first row relative to the group start.
+RD_HD int dw_group_block(const Tile& tl, int kb, int* row) {
+  const int rem = (tl.re - tl.rs) - (tl.nkb - 1) * kBK;
+  *row = rem - kBK + kb * kBK;
+  return kb == 0 ? (kBK - rem) >> 4 : 0;
 }
 
 // Zero fill: the 16-byte units [u0, u1) of the zero rows that one CTA writes.

@@ -5,8 +5,8 @@
  * Every entry point takes plain device pointers and sizes, enqueues work on
  * the caller's CUDA stream and returns at once.  The library never
  * synchronises, never copies device data to the host and allocates nothing
- * per call; group_sizes and limit stay on the device and are read by the
- * kernels themselves.  A call can therefore be captured in a CUDA graph,
+ * (the dw calls can use a small workspace the caller provides); group_sizes
+ * and limit stay on the device and are read by the kernels themselves.  A call can therefore be captured in a CUDA graph,
  * and replays follow device-side changes to group_sizes and limit.  The
  * first call of each entry point in a process sets a kernel attribute
  * (dynamic shared memory size); make it before a stream capture begins.
@@ -47,6 +47,7 @@
 #ifndef RD_H_
 #define RD_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -161,13 +162,38 @@ rd_status rd_ragged_dot_trans_rhs_glu_bwd(const void* d_out, const void* rhs, co
  * matmuls skip rows outside the groups and past limit).
  *
  *   x [m, k] bf16, y [m, n] bf16, out [g_local, k, n] bf16 (f32 accumulated).
+ *   workspace        device scratch of at least the size rd_trans_ragged_dot_
+ *                    workspace_size reports for the current device, 128-byte
+ *                    aligned, or NULL.  With it the kernel builds, per group,
+ *                    TMA descriptors whose rows are exactly the group's rows
+ *                    (rows outside the group then arrive as zeros); without
+ *                    it the rows of each group's first K block that precede
+ *                    the group are zeroed in shared memory, which is slower
+ *                    when group sizes are not multiples of 16.  The results
+ *                    agree within the stated accuracy (only the f32
+ *                    summation order differs).  The workspace is the call's
+ *                    own until the call completes on its stream: calls that
+ *                    may run at the same time need separate workspaces.  The
+ *                    library never reads what the workspace held before.
+ *   workspace_bytes  its size in bytes (ignored when workspace is NULL).
  *   Other arguments as rd_ragged_dot.
- * Requires k % 8 == 0, n % 8 == 0, 16-byte aligned pointers, no overlap.
+ * Requires k % 8 == 0, n % 8 == 0, 16-byte aligned pointers, no overlap
+ * (the workspace included); RD_ERR_INVALID_ARG for a workspace that is too
+ * small.
  */
 rd_status rd_trans_ragged_dot(const void* x, const void* y, void* out, int64_t m, int64_t k,
                               int64_t n, const int32_t* group_sizes, int32_t g_total,
                               int32_t group_offset, int32_t g_local, const int32_t* limit,
-                              int32_t* status, rd_stream_t stream);
+                              void* workspace, size_t workspace_bytes, int32_t* status,
+                              rd_stream_t stream);
+
+/*
+ * rd_trans_ragged_dot_workspace_size -- the workspace rd_trans_ragged_dot and
+ * rd_trans_ragged_dot_f32 take on the current device: 2 KB per SM (the
+ * per-group TMA descriptors of each CTA).  RD_ERR_INVALID_ARG for a NULL
+ * pointer, RD_ERR_UNSUPPORTED on a device other than sm_103.
+ */
+rd_status rd_trans_ragged_dot_workspace_size(size_t* bytes);
 
 /*
  * rd_trans_ragged_dot_f32 -- per-group weight gradient kept in f32, optionally
@@ -178,14 +204,15 @@ rd_status rd_trans_ragged_dot(const void* x, const void* y, void* out, int64_t m
  * form rounds once, to nearest.  SkyRL PR #867 (_gpu_trans_ragged_dot_fwd
  * separates acc_dtype = f32 from the compute dtype).
  *
- *   x [m, k] bf16, y [m, n] bf16, out [g_local, k, n] f32.  Other arguments as
- *   rd_trans_ragged_dot.  Calls that accumulate into the same buffer must be
- *   ordered on one stream.
+ *   x [m, k] bf16, y [m, n] bf16, out [g_local, k, n] f32.  Other arguments
+ *   (the workspace included) as rd_trans_ragged_dot.  Calls that accumulate
+ *   into the same buffer must be ordered on one stream.
  */
 rd_status rd_trans_ragged_dot_f32(const void* x, const void* y, float* out, int64_t m, int64_t k,
                                   int64_t n, const int32_t* group_sizes, int32_t g_total,
                                   int32_t group_offset, int32_t g_local, const int32_t* limit,
-                                  int32_t accumulate, int32_t* status, rd_stream_t stream);
+                                  int32_t accumulate, void* workspace, size_t workspace_bytes,
+                                  int32_t* status, rd_stream_t stream);
 
 /*
  * rd_glu_fwd -- SiLU-GLU forward over the valid rows of a fused buffer.

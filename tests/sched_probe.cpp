@@ -24,6 +24,16 @@ long long build(int op, const int32_t* sizes, int g_total, int m, int limit, int
   }
   bound[g_total] = clamp_boundary(run, L);
   long long t = 0;
+  if (op == kOpDw) {
+    // the group order of the dw tiles: groups without rows first
+    int p = 0;
+    for (int j = 0; j < gl; ++j)
+      if (group_is_empty(bound, off, j)) tile_start[p++] = j;
+    for (int j = 0; j < gl; ++j)
+      if (!group_is_empty(bound, off, j)) tile_start[p++] = j;
+    for (int j = 0; j < gl; ++j) t += tiles_of_group(op, 0, 0, tm, n_tiles, dw_m_tiles);
+    return t;
+  }
   for (int j = 0; j < gl; ++j) {
     tile_start[j] = static_cast<int32_t>(t);
     t += tiles_of_group(op, bound[off + j], bound[off + j + 1], tm, n_tiles, dw_m_tiles);
@@ -98,6 +108,18 @@ void sched_dw_block(int rs, int re, int kb, int32_t* out) {
   out[1] = kk0;
   out[2] = z0;
   out[3] = z1;
+}
+
+// dw through per-group maps, block kb of a group of `cnt` rows: out = (first
+// row relative to the group, first 16-row step issued).
+void sched_dw_group_block(int cnt, int kb, int32_t* out) {
+  Tile tl{};
+  tl.rs = 0;
+  tl.re = cnt;
+  tl.nkb = (cnt + kBK - 1) / kBK;
+  int row;
+  out[1] = dw_group_block(tl, kb, &row);
+  out[0] = row;
 }
 
 // The zero-fill share [u0, u1) of one CTA (unit, and sub = the CTA in a pair).

@@ -124,6 +124,12 @@ def run_dx(rd, m, k, n, sizes, off=0, gl=None, limit=None, seed=0):
 
 
 def run_dw(rd, m, k, n, sizes, off=0, gl=None, limit=None, seed=0):
+    """dw through both forms: per-group maps (a workspace) and in-smem edge zeroing (none)."""
+    for ws in ("auto", None):
+        _run_dw(rd, m, k, n, sizes, off, gl, limit, seed, ws)
+
+
+def _run_dw(rd, m, k, n, sizes, off, gl, limit, seed, ws):
     rng = np.random.default_rng(seed)
     gl = len(sizes) - off if gl is None else gl
     x = _normal(rng, (m, k))
@@ -140,7 +146,7 @@ def run_dw(rd, m, k, n, sizes, off=0, gl=None, limit=None, seed=0):
     buf.view(torch.int16).fill_(SENT)
     out = buf[:gl]
     rd.trans_ragged_dot(x_dev.to(DEV), y_dev.to(DEV), _i32(sizes), group_offset=off, g_local=gl,
-                        limit=None if limit is None else _i32([limit]), out=out)
+                        limit=None if limit is None else _i32([limit]), out=out, workspace=ws)
     torch.cuda.synchronize()
     assert np.all(obf.torch_bf16_bits(buf[gl]) == SENT), "the guard block after dw was written"
     got = _f64(out)
@@ -153,7 +159,7 @@ def run_dw(rd, m, k, n, sizes, off=0, gl=None, limit=None, seed=0):
             continue
         rows = slice(b[off + j], b[off + j + 1])
         tol = gemm_tol(ref[j], cnt, np.abs(x64[rows]).max(), np.abs(y64[rows]).max())
-        assert_close(got[j], ref[j], tol, f"dw group {j} ({cnt} rows)")
+        assert_close(got[j], ref[j], tol, f"dw group {j} ({cnt} rows, workspace {ws})")
 
 
 # ------------------------------------------------------------------ forward
@@ -399,6 +405,29 @@ def test_fused_glu_backward_special_gates(rd_lib):
 DW_SIZES = [0, 1, 63, 64, 65, 200, 0, 130]   # sum 523
 
 
+def test_dw_group_sizes_around_16_and_64(rd_lib):
+    """Group sizes at and around multiples of 16 and 64 (the K step and K block), both forms."""
+    sizes = [15, 16, 17, 47, 48, 49, 79, 80, 81, 127, 128, 129, 1, 2, 190, 191, 192, 193]
+    run_dw(rd_lib, sum(sizes) + 5, 128, 256, sizes, seed=77)
+
+
+def test_dw_workspace_checks(rd_lib):
+    """A workspace that is too small, misaligned or overlapping an operand is refused."""
+    x = torch.zeros((64, 128), dtype=torch.bfloat16, device=DEV)
+    y = torch.zeros((64, 256), dtype=torch.bfloat16, device=DEV)
+    need = rd_lib.dw_workspace_bytes()
+    assert need > 0 and need % 128 == 0
+    small = torch.empty(need - 128, dtype=torch.uint8, device=DEV)
+    with pytest.raises(rd_lib.RdError):
+        rd_lib.trans_ragged_dot(x, y, _i32([30, 34]), workspace=small)
+    big = torch.empty(need + 256, dtype=torch.uint8, device=DEV)
+    with pytest.raises(rd_lib.RdError):
+        rd_lib.trans_ragged_dot(x, y, _i32([30, 34]), workspace=big[64:64 + need])
+    with pytest.raises(rd_lib.RdError):   # the workspace overlaps the output
+        out = big[:2 * 128 * 256 * 2].view(torch.bfloat16).view(2, 128, 256)
+        rd_lib.trans_ragged_dot(x, y, _i32([30, 34]), out=out, workspace=big)
+
+
 @pytest.mark.parametrize("m,k,n,off,gl,limit", [(600, 136, 264, 0, 8, None), (600, 128, 256, 2, 5, 400),
                                                 (523, 264, 72, 0, 8, 523), (600, 64, 520, 3, 4, 130)])
 def test_dw(rd_lib, m, k, n, off, gl, limit):
@@ -406,6 +435,11 @@ def test_dw(rd_lib, m, k, n, off, gl, limit):
 
 
 def run_dw_f32(rd, m, k, n, sizes, off=0, gl=None, limit=None, seed=0, accumulate=False):
+    for ws in ("auto", None):
+        _run_dw_f32(rd, m, k, n, sizes, off, gl, limit, seed, accumulate, ws)
+
+
+def _run_dw_f32(rd, m, k, n, sizes, off, gl, limit, seed, accumulate, ws):
     from oracle import ragged
     rng = np.random.default_rng(seed)
     gl = len(sizes) - off if gl is None else gl
@@ -427,7 +461,7 @@ def run_dw_f32(rd, m, k, n, sizes, off=0, gl=None, limit=None, seed=0, accumulat
         out.fill_(float("nan"))
     rd.trans_ragged_dot_f32(x_dev.to(DEV), y_dev.to(DEV), _i32(sizes), group_offset=off, g_local=gl,
                             limit=None if limit is None else _i32([limit]), out=out,
-                            accumulate=accumulate)
+                            accumulate=accumulate, workspace=ws)
     torch.cuda.synchronize()
     assert bool((buf[gl] == 5.5).all()), "the guard block after dw was written"
     got = out.cpu().numpy().astype(np.float64)

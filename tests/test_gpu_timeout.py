@@ -23,7 +23,7 @@ def _inputs(op, seed):
     a 1 ns bound certainly runs out whatever the resolution of the global timer."""
     from workloads import normal_bf16_np
     rng = np.random.default_rng(seed)
-    if op == "dw":
+    if op.startswith("dw"):
         m, k, n, sizes = 16384, 256, 512, [4096, 4100, 4000, 4188]
     else:
         m, k, n, sizes = 1024, 8192, 512, [256, 300, 200, 268]
@@ -40,11 +40,14 @@ def _call(rd, op, a, w, do, gs, status):
         return rd.ragged_dot(a, w, gs, status=status)
     if op == "dx":
         return rd.ragged_dot_trans_rhs(do, w, gs, status=status)
+    if op == "dw_nows":
+        return rd.trans_ragged_dot(a, do, gs, status=status, workspace=None)
     return rd.trans_ragged_dot(a, do, gs, status=status)
 
 
 @pytest.mark.parametrize("variant,op", [("single", "fwd"), ("pair", "fwd"), ("single", "dx"),
-                                        ("pair", "dx"), ("single", "dw"), ("pair", "dw")])
+                                        ("pair", "dx"), ("single", "dw"), ("pair", "dw"),
+                                        ("single", "dw_nows"), ("pair", "dw_nows")])
 def test_timeout_unwinds_and_reports(rd_lib, variant, op):
     v = rd_lib.VARIANT_PAIR if variant == "pair" else rd_lib.VARIANT_SINGLE
     a, w, do, sizes = _inputs(op, 1)

@@ -48,6 +48,7 @@ def probe(tmp_path_factory):
         [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_longlong]
     lib.sched_dw_block.argtypes = [ctypes.c_int] * 3 + [ctypes.c_void_p]
     lib.sched_zero_share.argtypes = [ctypes.c_ulonglong] + [ctypes.c_int] * 5 + [ctypes.c_void_p]
+    lib.sched_dw_group_block.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
     return lib
 
 
@@ -138,6 +139,10 @@ def test_dw_blocks_feed_each_group_row_once(probe, tm):
         keys = {(int(j), int(mi), int(ni)) for j, mi, ni in tiles[:, :3]}
         assert keys == {(j, mi, ni) for j in range(gl) for mi in range(dw_m_tiles)
                         for ni in range(n_tiles)}
+        # groups without rows come first in the tile order, each part in index order
+        seq = [int(j) for j in tiles[::n_tiles * dw_m_tiles, 0]]
+        empty = [j for j in range(gl) if b[off + j + 1] == b[off + j]]
+        assert seq == empty + [j for j in range(gl) if j not in empty]
         checked = set()
         for (j, _, _, rs, re, _, nkb, _, _) in tiles.tolist():
             if j in checked:
@@ -153,6 +158,26 @@ def test_dw_blocks_feed_each_group_row_once(probe, tm):
                 # steps before kk0 are not issued; rows [z0, z1) are zeroed
                 fed += list(range(row0 + z1, row0 + 64))
             assert sorted(fed) == list(range(rs, re)), f"group {j}: rows fed to the MMA"
+
+
+def test_dw_group_map_blocks(probe):
+    """dw through per-group maps: the blocks end at the group end; rows above the group
+    start (negative, out of the map's bounds, zero-filled) lie only in the first block;
+    after the skipped whole steps every group row is fed once and no row past it."""
+    out = np.zeros(2, np.int32)
+    for cnt in list(range(1, 300)) + [1023, 1024, 1025, 1170, 4096]:
+        nkb = -(-cnt // 64)
+        fed = []
+        for kb in range(nkb):
+            probe.sched_dw_group_block(cnt, kb, out.ctypes.data)
+            row, kk0 = int(out[0]), int(out[1])
+            assert row + 64 <= cnt, "a block reads past the group"
+            if kb > 0:
+                assert row >= 0 and kk0 == 0
+            else:
+                assert -64 < row <= 0 and row + 16 * kk0 > -16 and row + 16 * kk0 <= 0
+            fed += [r for r in range(row + 16 * kk0, row + 64) if r >= 0]
+        assert fed == list(range(cnt))
 
 
 def test_zero_fill_shares_partition_the_zero_rows(probe):
