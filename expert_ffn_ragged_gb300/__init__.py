@@ -13,6 +13,7 @@ Functions (same names as the C ABI, without the ``rd_`` prefix):
 * ``trans_ragged_dot(x, y, group_sizes, ...)``           -> out [g_local, k, n]
 * ``trans_ragged_dot_f32(x, y, group_sizes, ..., accumulate=False)`` -> f32 out [g_local, k, n]
 * ``dw_workspace_bytes(device)``                         -> the dw calls' workspace size
+* ``trans_ragged_dot_no_alloc(x, y, group_sizes, ...)``  -> dw with no allocation (library scratch)
 * ``glu_fwd(fused, limit=None)``                         -> out [rows, f]
 * ``glu_bwd(fused, d_out, limit=None)``                  -> d_fused [rows, 2f]
 * ``unsort_bwd_rows(g, y, w, limit=None)``                -> (grad [rows, hidden], dot [rows])
@@ -31,7 +32,7 @@ from typing import Optional
 
 __all__ = [
     "load", "lib_path", "ragged_dot", "ragged_dot_trans_rhs", "ragged_dot_trans_rhs_glu_bwd",
-    "trans_ragged_dot", "trans_ragged_dot_f32", "dw_workspace_bytes",
+    "trans_ragged_dot", "trans_ragged_dot_f32", "trans_ragged_dot_no_alloc", "dw_workspace_bytes",
     "glu_fwd", "glu_bwd", "unsort_bwd_rows", "RdError", "EPI_NONE", "EPI_SILU_GLU",
     "STATUS_NEG_SIZE", "STATUS_OVERFLOW", "STATUS_TIMEOUT", "MAX_GROUPS",
     "VARIANT_AUTO", "VARIANT_SINGLE", "VARIANT_PAIR", "set_tuning", "get_tuning", "tuning",
@@ -85,6 +86,8 @@ def load():
     sz = ctypes.c_size_t
     lib.rd_trans_ragged_dot.argtypes = grouped + [vp, sz, ip, vp]
     lib.rd_trans_ragged_dot_f32.argtypes = grouped + [i32, vp, sz, ip, vp]
+    lib.rd_trans_ragged_dot_no_alloc.argtypes = grouped + [ip, vp]
+    lib.rd_trans_ragged_dot_no_alloc.restype = ctypes.c_int
     lib.rd_trans_ragged_dot_workspace_size.argtypes = [ctypes.c_void_p]
     lib.rd_trans_ragged_dot_workspace_size.restype = ctypes.c_int
     lib.rd_glu_fwd.argtypes = [vp, vp, i64, i64, ip, vp]
@@ -402,6 +405,35 @@ def trans_ragged_dot(x, y, group_sizes, group_offset: int = 0, g_local: Optional
                                        _ptr(ws), 0 if ws is None else ws.numel(), _ptr(status),
                                        _stream(stream, dev))
     _check(code, "rd_trans_ragged_dot")
+    return out
+
+
+def trans_ragged_dot_no_alloc(x, y, group_sizes, group_offset: int = 0,
+                              g_local: Optional[int] = None, limit=None, out=None, status=None,
+                              stream=None):
+    """trans_ragged_dot for callers that cannot allocate device memory at the call.
+
+    The same per-group-descriptor dw as trans_ragged_dot with a workspace, its
+    scratch taken from an array inside the library (see
+    rd_trans_ragged_dot_no_alloc: up to 256 SMs; calls that overlap on the GPU
+    race on the array; make the first call on a device outside stream capture).
+    Pass ``out`` to allocate nothing at all.
+    """
+    import torch
+
+    lib = load()
+    m, k, n, g_local = _dw_args(x, y, group_sizes, group_offset, g_local, limit, status)
+    dev = x.device
+    if out is None:
+        out = torch.empty((g_local, k, n), dtype=torch.bfloat16, device=dev)
+    _out(out, (g_local, k, n), torch.bfloat16)
+    _same_device(dev, y, out, group_sizes, limit, status)
+    with _on_device(dev):
+        code = lib.rd_trans_ragged_dot_no_alloc(_ptr(x), _ptr(y), _ptr(out), m, k, n,
+                                                _ptr(group_sizes), group_sizes.numel(),
+                                                group_offset, g_local, _ptr(limit), _ptr(status),
+                                                _stream(stream, dev))
+    _check(code, "rd_trans_ragged_dot_no_alloc")
     return out
 
 

@@ -583,6 +583,57 @@ extern "C" rd_status rd_unsort_bwd_rows(const void* g, const void* y, const floa
              : RD_ERR_CUDA;
 }
 
+// ------------------------------------------------ dw without any allocation
+// Some callers cannot allocate device memory at the point where they run the
+// weight gradient: code inside an allocator's own callbacks, a runtime that
+// owns every allocation and hands out no scratch, or a process that must not
+// grow its footprint once set up.  For them rd_trans_ragged_dot_no_alloc runs
+// the per-group-descriptor form of the dw kernel with its scratch in this
+// file-scope array, which every GPU that loads the library holds until exit.
+// It covers devices of up to kNoAllocMaxSms SMs (2 KB of descriptors per SM).
+constexpr int kNoAllocMaxSms = 256;
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(kNoAllocMaxSms) * kMapBytesPerCta;
+static __device__ __align__(256) unsigned char g_no_alloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+// The array's device address on the current device.  In host code the array's
+// name only stands in for the symbol: its address must come from the runtime,
+// once per device, with that device current.
+rd_status no_alloc_scratch(void** ptr) {
+  static std::mutex mu;
+  static void* addr[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RD_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return RD_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_no_alloc_scratch) != cudaSuccess || p == nullptr)
+      return RD_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return RD_OK;
+}
+}  // namespace
+
+extern "C" rd_status rd_trans_ragged_dot_no_alloc(const void* x, const void* y, void* out, int64_t m,
+                                                  int64_t k, int64_t n, const int32_t* group_sizes,
+                                                  int32_t g_total, int32_t group_offset,
+                                                  int32_t g_local, const int32_t* limit,
+                                                  int32_t* status, rd_stream_t stream) {
+  // the argument checks every dw call makes, before any CUDA call
+  rd_status st = check_groups(m, k, n, group_sizes, g_total, group_offset, g_local, limit, status);
+  if (st != RD_OK) return st;
+  int sms = 0;
+  if ((st = current_device(&sms)) != RD_OK) return st;
+  if (sms > kNoAllocMaxSms) return RD_ERR_UNSUPPORTED;  // more CTAs than the array has room for
+  void* scratch = nullptr;
+  if ((st = no_alloc_scratch(&scratch)) != RD_OK) return st;
+  return trans_ragged_impl(x, y, out, m, k, n, group_sizes, g_total, group_offset, g_local, limit,
+                           kEpiNone, scratch, kNoAllocScratchBytes, status, stream);
+}
+
 extern "C" rd_status rd_set_tuning(const rd_tuning* t) {
   if (t == nullptr) {
     g_variant.store(RD_VARIANT_AUTO);

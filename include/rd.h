@@ -215,6 +215,34 @@ rd_status rd_trans_ragged_dot_f32(const void* x, const void* y, float* out, int6
                                   int32_t* status, rd_stream_t stream);
 
 /*
+ * rd_trans_ragged_dot_no_alloc -- rd_trans_ragged_dot for callers that cannot
+ * allocate device memory.  The source pages have no counterpart: this entry
+ * point exists for code that has no way to provide the workspace, such as a
+ * caller running inside a memory allocator's own callbacks, a runtime that
+ * owns every device allocation and hands out no scratch, or a process that
+ * must not grow its footprint after set-up.  It computes what
+ * rd_trans_ragged_dot computes with a workspace (the per-group-descriptor
+ * form), taking its 2 KB of descriptors per SM from a 512 KB array inside the
+ * library that every GPU loading the library holds until the process exits;
+ * it allocates nothing and calls no allocating routine.
+ *
+ *   Arguments as rd_trans_ragged_dot, without the workspace.
+ *   Limit: devices of up to 256 SMs; on a larger device it returns
+ *   RD_ERR_UNSUPPORTED and enqueues nothing.
+ *   Set-up: the first call on each device asks the CUDA runtime for the
+ *   array's device address (once per device, with that device current); make
+ *   that first call before any stream capture on the device.
+ *   Sharing: every call on a device uses the same array, which keeps the last
+ *   call's descriptors; no call reads what an earlier one left there.  Calls
+ *   whose kernels overlap on the GPU (other streams, other threads) race on
+ *   the array and give wrong results: order such calls on one stream.
+ */
+rd_status rd_trans_ragged_dot_no_alloc(const void* x, const void* y, void* out, int64_t m,
+                                       int64_t k, int64_t n, const int32_t* group_sizes,
+                                       int32_t g_total, int32_t group_offset, int32_t g_local,
+                                       const int32_t* limit, int32_t* status, rd_stream_t stream);
+
+/*
  * rd_glu_fwd -- SiLU-GLU forward over the valid rows of a fused buffer.
  *   out[r, c] = bf16( g / (1 + exp(-g)) * u ),  g = fused[r, c], u = fused[r, f + c],
  *   for r < L; rows >= L of out are not written and of fused not read.

@@ -31,8 +31,8 @@ def test_header_declares_the_abi():
     assert _declared() == sorted([
         "rd_glu_bwd", "rd_glu_fwd", "rd_ragged_dot", "rd_ragged_dot_trans_rhs",
         "rd_get_tuning", "rd_ragged_dot_trans_rhs_glu_bwd", "rd_set_tuning", "rd_status_string",
-        "rd_trans_ragged_dot", "rd_trans_ragged_dot_f32", "rd_trans_ragged_dot_workspace_size",
-        "rd_unsort_bwd_rows"])
+        "rd_trans_ragged_dot", "rd_trans_ragged_dot_f32", "rd_trans_ragged_dot_no_alloc",
+        "rd_trans_ragged_dot_workspace_size", "rd_unsort_bwd_rows"])
 
 
 class _Tuning(ctypes.Structure):
@@ -137,6 +137,11 @@ def test_other_entry_points_check_arguments(lib):
     # a workspace must be 128-byte aligned
     assert f(P, P * 0x100, P * 0x10000, 16, 64, 64, P * 0x1000000, 4, 0, 4, None, P * 0x3000 + 64, 1 << 20,
              None, None) == RD_ERR_UNSUPPORTED
+    f = lib.rd_trans_ragged_dot_no_alloc
+    f.restype = ctypes.c_int
+    f.argtypes = [v, v, v, i64, i64, i64, v, i32, i32, i32, v, v, v]
+    assert f(P, P * 0x100, P * 0x10000, 16, 64, 64, None, 4, 0, 4, None, None, None) == RD_ERR_INVALID_ARG
+    assert f(P, P * 0x100, P * 0x10000, 16, 60, 64, P * 0x1000000, 4, 0, 4, None, None, None) == RD_ERR_UNSUPPORTED
     lib.rd_trans_ragged_dot_workspace_size.restype = ctypes.c_int
     lib.rd_trans_ragged_dot_workspace_size.argtypes = [v]
     assert lib.rd_trans_ragged_dot_workspace_size(None) == RD_ERR_INVALID_ARG
