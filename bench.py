@@ -258,10 +258,33 @@ def run_ops(rd, device, stream, peaks):
     from workloads import backward_pair, decode_fwd, normal_bf16, packed_glu_fwd, tiny_fwd
 
     P = peaks["bf16_tflops"] * 1e12
+    PS = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * 1e12
     BW = peaks["hbm_gbs"] * 1e9
     res = {}
 
     spread = []  # (entry, key prefix, p10 us, p90 us) of each timed call
+
+    def clock_probe(fn, entry, flops, seconds=0.25):
+        """The SM clock while the call runs back to back (sampled by nvidia-smi), and the
+        fraction of the sustained bf16 peak (the cuBLAS figure under the power cap).
+
+        The timed calls run first, on a GPU that is already warm; this loop runs the
+        same call for a quarter of a second right after, long enough for several
+        clock samples, and only reports the clock it ran at.
+        """
+        with ClockSampler(device.index if device.index is not None else 0, period_ms=10) as clk:
+            clk.mark_start()
+            t0 = time.time()
+            while time.time() - t0 < seconds:
+                for _ in range(5):
+                    fn()
+                torch.cuda.synchronize()
+            clk.mark_end()
+        c = clk.summary()
+        r = res[entry]
+        r["mhz"] = c["sm_mhz"]
+        r["power_cap"] = "sw_power_cap" in c["reasons"]
+        r["frac_sustained"] = flops / PS / (r["us"] * 1e-6)
 
     def med(fn, steps=20, warmup=3, entry=None, prefix=""):
         per, _ = time_launches(fn, steps, warmup, stream)
@@ -283,12 +306,13 @@ def run_ops(rd, device, stream, peaks):
         F = 2.0 * rows * w.k * w.n
         zero_rows = w.limit - rows
         B = rows * w.k * 2 + w.g_local * w.k * w.n * 2 + w.limit * (w.n // 2) * 2 + 4 * w.g_total
-        t = med(lambda: rd.ragged_dot(lhs, rhs, gs, w.group_offset, lim, rd.EPI_SILU_GLU, out),
-                entry="packed_glu_fwd")
+        glu_call = lambda: rd.ragged_dot(lhs, rhs, gs, w.group_offset, lim, rd.EPI_SILU_GLU, out)
+        t = med(glu_call, entry="packed_glu_fwd")
         res["packed_glu_fwd"] = {"us": t * 1e6, "tflops": F / t / 1e12, "gbs": B / t / 1e9,
                                  "bound": "hbm" if B / BW > F / P else "tensor",
                                  "frac": max(F / P, B / BW) / t,
                                  "local_rows": rows, "zero_rows": zero_rows}
+        clock_probe(glu_call, "packed_glu_fwd", F)
         # standalone GLU on the same packed buffer shape
         fused = normal_bf16((w.m, 2 * 1024), 1.0, 32, device)
         gout = torch.empty((w.m, 1024), dtype=torch.bfloat16, device=device)
@@ -349,18 +373,22 @@ def run_ops(rd, device, stream, peaks):
         dw = torch.empty((w.g_total, w.k, w.n), dtype=torch.bfloat16, device=device)
         F = 2.0 * w.m * w.k * w.n
         live = int((w.group_sizes > 0).sum())
-        t = med(lambda: rd.ragged_dot_trans_rhs(do, wt, gs, out=dx), entry="dx")
+        dx_call = lambda: rd.ragged_dot_trans_rhs(do, wt, gs, out=dx)
+        t = med(dx_call, entry="dx")
         B = w.m * w.n * 2 + live * w.k * w.n * 2 + w.m * w.k * 2
         res["dx"] = {"us": t * 1e6, "tflops": F / t / 1e12,
                      "bound": "hbm" if B / BW > F / P else "tensor",
                      "frac": max(F / P, B / BW) / t}
+        clock_probe(dx_call, "dx", F)
         # dw through per-group tensor maps, in a workspace allocated once
         ws = torch.empty(rd.dw_workspace_bytes(device), dtype=torch.uint8, device=device)
-        t = med(lambda: rd.trans_ragged_dot(x, do, gs, out=dw, workspace=ws), entry="dw")
+        dw_call = lambda: rd.trans_ragged_dot(x, do, gs, out=dw, workspace=ws)
+        t = med(dw_call, entry="dw")
         B = w.m * w.k * 2 + w.m * w.n * 2 + w.g_total * w.k * w.n * 2
         res["dw"] = {"us": t * 1e6, "tflops": F / t / 1e12,
                      "bound": "hbm" if B / BW > F / P else "tensor",
                      "frac": max(F / P, B / BW) / t}
+        clock_probe(dw_call, "dw", F)
         del dx, dw
         torch.cuda.empty_cache()
         # dw kept in f32 (stored, then added into an existing gradient buffer)
@@ -375,6 +403,8 @@ def run_ops(rd, device, stream, peaks):
             res[key] = {"us": t * 1e6, "tflops": F / t / 1e12,
                         "bound": "tensor" if F / P >= B / BW else "hbm",
                         "frac": max(F / P, B / BW) / t}
+            if not acc:
+                clock_probe(lambda: rd.trans_ragged_dot_f32(x, do, gs, out=dw32, workspace=ws), key, F)
         del x, do, wt, dw32, ws
         torch.cuda.empty_cache()
 
@@ -458,7 +488,9 @@ def compact_ops(res):
     backward pair (dx, dw, dw in f32, accumulated f32), c5 the decode pair in one
     graph (skewed / uniform routing), the standalone GLU and unsort passes on the
     packed buffer, the fused dx + GLU backward, and the expert-FFN graph by token
-    count ([us, frac, bound]).  p10 / p90 are given for the five configs.
+    count ([us, frac, bound]).  p10 / p90 are given for the five configs; the
+    tensor-bound GEMM rows add the SM clock under their own sustained load (mhz),
+    their fraction of the sustained bf16 peak (fs) and the power-cap flag (cap).
     """
     b = {"tensor": "t", "hbm": "h", "latency": "l"}
     out = {}
@@ -475,6 +507,12 @@ def compact_ops(res):
             e["p10"], e["p90"] = _sig(p10, 3), _sig(p90, 3)
         for k_out, k_in in extra:
             e[k_out] = _sig(r[k_in])
+        if r.get("mhz") is not None:
+            # the SM clock under this call's sustained load, the fraction of the
+            # sustained peak, and whether the power cap was holding the clock down
+            e["mhz"] = int(round(r["mhz"]))
+            e["fs"] = _sig(r["frac_sustained"], 3)
+            e["cap"] = int(bool(r.get("power_cap")))
         out[key] = e
 
     if "tiny" in res:
