@@ -114,59 +114,81 @@ def _check(code: int, what: str):
         raise RdError(code, f"{what}: {msg}")
 
 
+_torch_module = None
+
+
+def _torch():
+    """torch, imported once (a call's host work is part of its latency)."""
+    global _torch_module
+    if _torch_module is None:
+        import torch
+
+        _torch_module = torch
+    return _torch_module
+
+
 def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def _stream(stream, device):
-    import torch
+_raw_stream = None
 
+
+def _stream(stream, device):
+    """The raw cudaStream_t of ``stream`` (default: the device's current stream)."""
+    global _raw_stream
+    torch = _torch()
     if stream is None:
+        if _raw_stream is None:
+            # the current stream's handle without building a Stream object (the
+            # public route costs ~2 us a call); fall back to it where absent
+            _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+        if _raw_stream:
+            return _raw_stream(device.index if device.index is not None
+                               else torch.cuda.current_device())
         stream = torch.cuda.current_stream(device)
     elif stream.device != device:
         raise ValueError("stream is on another device than the tensors")
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 class _on_device:
     """Make ``device`` current for the call (the library launches on the current device)."""
 
-    def __init__(self, device):
-        import torch
+    __slots__ = ("idx", "prev")
 
-        self.idx = device.index if device.index is not None else torch.cuda.current_device()
+    def __init__(self, device):
+        self.idx = device.index if device.index is not None else _torch().cuda.current_device()
         self.prev = None
 
     def __enter__(self):
-        import torch
-
+        torch = _torch()
         cur = torch.cuda.current_device()
         if cur != self.idx:
             self.prev = cur
             torch.cuda.set_device(self.idx)
 
     def __exit__(self, *exc):
-        import torch
-
         if self.prev is not None:
-            torch.cuda.set_device(self.prev)
+            _torch().cuda.set_device(self.prev)
 
 
 def _same_device(device, *tensors):
+    idx = device.index if device.index is not None else _torch().cuda.current_device()
     for t in tensors:
-        if t is not None and t.device != device:
+        if t is not None and t.get_device() != idx:
             raise ValueError(f"all tensors of a call must be on {device} (one is on {t.device})")
 
 
 def _bf16_2d(t, name):
-    import torch
+    torch = _torch()
 
     if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous 2-D bf16 CUDA tensor")
 
 
 def _bf16_3d(t, name, what):
-    import torch
+    torch = _torch()
 
     if t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous {what} bf16 CUDA tensor")
@@ -180,14 +202,14 @@ def _out(t, shape, dtype, name="out"):
 
 
 def _scalar_i32(t, name):
-    import torch
+    torch = _torch()
 
     if t is not None and (t.dtype != torch.int32 or t.numel() != 1 or not t.is_cuda):
         raise ValueError(f"{name} must be a one-element int32 CUDA tensor")
 
 
 def _group_args(group_sizes, limit, status):
-    import torch
+    torch = _torch()
 
     if (group_sizes.dtype != torch.int32 or group_sizes.dim() != 1 or not group_sizes.is_cuda
             or not group_sizes.is_contiguous()):
@@ -252,7 +274,7 @@ class tuning:
 def ragged_dot(lhs, rhs, group_sizes, group_offset: int = 0, limit=None, epilogue: int = EPI_NONE,
                out=None, status=None, stream=None):
     """Grouped forward out[i] = lhs[i] @ rhs[group(i) - group_offset] (see rd_ragged_dot)."""
-    import torch
+    torch = _torch()
 
     lib = load()
     _bf16_2d(lhs, "lhs")
@@ -279,7 +301,7 @@ def ragged_dot(lhs, rhs, group_sizes, group_offset: int = 0, limit=None, epilogu
 def ragged_dot_trans_rhs(lhs, rhs, group_sizes, group_offset: int = 0, limit=None, out=None,
                          status=None, stream=None):
     """out[i] = lhs[i] @ rhs[group(i) - group_offset]^T; lhs [m, n], rhs [g_local, k, n]."""
-    import torch
+    torch = _torch()
 
     lib = load()
     _bf16_2d(lhs, "lhs")
@@ -308,7 +330,7 @@ def ragged_dot_trans_rhs_glu_bwd(d_out, rhs, fused, group_sizes, group_offset: i
 
     d_out [m, n], rhs [g_local, f, n] (down weights), fused [m, 2f] (saved gate | up).
     """
-    import torch
+    torch = _torch()
 
     lib = load()
     _bf16_2d(d_out, "d_out")
@@ -338,7 +360,7 @@ _ws_bytes = {}
 
 def dw_workspace_bytes(device=None) -> int:
     """Bytes of the dw workspace (rd_trans_ragged_dot_workspace_size) on a CUDA device."""
-    import torch
+    torch = _torch()
 
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     if dev.index not in _ws_bytes:
@@ -353,7 +375,7 @@ def dw_workspace_bytes(device=None) -> int:
 
 def _dw_workspace(workspace, dev, stream):
     """The workspace argument of the dw calls: "auto" allocates one for this call."""
-    import torch
+    torch = _torch()
 
     if workspace is None:
         return None
@@ -389,7 +411,7 @@ def trans_ragged_dot(x, y, group_sizes, group_offset: int = 0, g_local: Optional
     workspace: "auto" (a workspace of dw_workspace_bytes() allocated for the
     call), None (the form without one), or a caller's uint8 CUDA tensor.
     """
-    import torch
+    torch = _torch()
 
     lib = load()
     m, k, n, g_local = _dw_args(x, y, group_sizes, group_offset, g_local, limit, status)
@@ -419,7 +441,7 @@ def trans_ragged_dot_no_alloc(x, y, group_sizes, group_offset: int = 0,
     race on the array; make the first call on a device outside stream capture).
     Pass ``out`` to allocate nothing at all.
     """
-    import torch
+    torch = _torch()
 
     lib = load()
     m, k, n, g_local = _dw_args(x, y, group_sizes, group_offset, g_local, limit, status)
@@ -445,7 +467,7 @@ def trans_ragged_dot_f32(x, y, group_sizes, group_offset: int = 0, g_local: Opti
     An accumulating call whose status reports STATUS_TIMEOUT has added some
     tiles and not others: its output is unusable (a retry would add twice).
     """
-    import torch
+    torch = _torch()
 
     lib = load()
     m, k, n, g_local = _dw_args(x, y, group_sizes, group_offset, g_local, limit, status)
@@ -469,7 +491,7 @@ def trans_ragged_dot_f32(x, y, group_sizes, group_offset: int = 0, g_local: Opti
 
 def glu_fwd(fused, limit=None, out=None, stream=None):
     """silu(gate) * up over the rows below limit of a fused [rows, 2f] buffer."""
-    import torch
+    torch = _torch()
 
     lib = load()
     _bf16_2d(fused, "fused")
@@ -488,7 +510,7 @@ def glu_fwd(fused, limit=None, out=None, stream=None):
 
 def glu_bwd(fused, d_out, limit=None, out=None, stream=None):
     """[d_gate | d_up] for the rows below limit; fused [rows, 2f], d_out [rows, f]."""
-    import torch
+    torch = _torch()
 
     lib = load()
     _bf16_2d(fused, "fused")
@@ -511,7 +533,7 @@ def glu_bwd(fused, d_out, limit=None, out=None, stream=None):
 
 def unsort_bwd_rows(g, y, w, limit=None, grad=None, dot=None, stream=None):
     """Weighted gradient bf16(f32(g) * w) and f32 row dot sum(g * y) over rows below limit."""
-    import torch
+    torch = _torch()
 
     lib = load()
     _bf16_2d(g, "g")
