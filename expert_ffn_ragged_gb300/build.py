@@ -3,7 +3,7 @@
 The translation units compile in parallel; the result lands in
 ``expert_ffn_ragged_gb300/_lib/librd.so``.  The CUDA runtime is linked
 statically, so the library loads on a machine without a GPU (the exported
-symbols can be checked there) and needs only the driver at run time.
+symbols can be checked there) and needs only the NVIDIA GPU driver at run time.
 """
 from __future__ import annotations
 

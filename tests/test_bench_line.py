@@ -1,9 +1,9 @@
 """The bench line on the host: the ops summary keeps every row and stays short.
 
-The driver keeps only the last 1500 characters of the bench's output, so the
-`ops` summary (the last key of the line) must carry every row of the hot path
-in well under that.  Built here from a result dict shaped like run_ops'
-output, with long floats everywhere, so no GPU is needed.
+A log that keeps only the last 1500 characters of the bench's output must
+still hold every row of the hot path, so the `ops` summary (the last key of
+the line) has to fit well inside that.  Built here from a result dict shaped
+like run_ops' output, with long floats everywhere, so no GPU is needed.
 """
 import json
 import os
