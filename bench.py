@@ -29,7 +29,7 @@ Also reported on the same line:
 
 --profile NAME runs a few launches of one workload for ncu (mixtral,
 mixtral_small, packed_glu, dx, dw, dw_f32acc, packed_dx_glu_bwd, glu_fwd,
-glu_bwd, unsort, decode).
+glu_bwd, unsort, decode, ffn4096_up).
 
 --impl reference times the oracle itself as the reference arm.
 Under torchrun (--gpus N) every rank runs an independent replica (no
@@ -917,6 +917,14 @@ def run_profile(args):
         def fn():
             rd.ragged_dot(lhs, up, gs, epilogue=rd.EPI_SILU_GLU, out=h)
             rd.ragged_dot(h, down, gs, out=o)
+    elif name == "ffn4096_up":
+        # the expert-FFN up projection (GLU) at 4096 tokens: ~256 rows per expert
+        w = workloads.expert_ffn(4096)
+        lhs = normal_bf16((w.m, w.k), 1.0, 63, device)
+        up = normal_bf16((w.g_total, w.k, w.n), 1.0 / w.k, 61, device)
+        gs = torch.tensor(w.group_sizes, dtype=torch.int32, device=device)
+        h = torch.empty((w.m, w.n // 2), dtype=torch.bfloat16, device=device)
+        fn = lambda: rd.ragged_dot(lhs, up, gs, epilogue=rd.EPI_SILU_GLU, out=h)
     else:
         raise SystemExit(f"unknown profile workload {name}")
     for _ in range(args.steps):
