@@ -22,10 +22,12 @@ Also reported on the same line:
                 forward/backward, unsort backward, the fused GLU backward
                 through the down projection, the tiny workload's latency, and
                 the expert FFN forward graph from 256 to 16384 tokens), each as
-                median time per call in us, fraction of its roofline and the
-                bound ("t" tensor, "h" HBM, "l" latency), with p10 / p90 for
-                the five configs; short keys and 3-4 significant digits keep
-                the whole line short.  --ops-json FILE writes the full figures.
+                time per call in us (calls back to back between two events,
+                the total divided by the calls, as for the headline), fraction
+                of its roofline and the bound ("t" tensor, "h" HBM, "l"
+                latency), with p10 / p90 of events around each call for the
+                five configs; short keys and 3-4 significant digits keep the
+                whole line short.  --ops-json FILE writes the full figures.
 
 --profile NAME runs a few launches of one workload for ncu (mixtral,
 mixtral_small, packed_glu, dx, dw, dw_f32acc, packed_dx_glu_bwd, glu_fwd,
@@ -286,12 +288,24 @@ def run_ops(rd, device, stream, peaks):
         r["power_cap"] = "sw_power_cap" in c["reasons"]
         r["frac_sustained"] = flops / PS / (r["us"] * 1e-6)
 
-    def med(fn, steps=20, warmup=3, entry=None, prefix=""):
+    def med(fn, steps=20, warmup=3, entry=None, prefix="", per_call=False):
+        """Seconds per call: `steps` calls back to back between two events, divided by
+        `steps` (as the headline's value), or with per_call the median of events around
+        each call (a single call's latency); the p10 / p90 spread comes from the loop
+        with events around every call."""
         per, _ = time_launches(fn, steps, warmup, stream)
         if entry is not None:
             q = statistics.quantiles(per, n=10)
             spread.append((entry, prefix, q[0] * 1e3, q[-1] * 1e3))
-        return statistics.median(per) * 1e-3
+        if per_call:
+            return statistics.median(per) * 1e-3
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            fn()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / steps * 1e-3
 
     with torch.cuda.stream(stream):
         # packed buffer forward + fused GLU, group_offset 16 of 64, limit 126156
@@ -450,7 +464,7 @@ def run_ops(rd, device, stream, peaks):
         # on an idle GPU the events around one call also hold the call's host work
         # (argument checks, tensor-map encoding); 20 launches replayed from a CUDA
         # graph give the device time of a launch alone
-        t_call = med(lambda: rd.ragged_dot(lhs, rhs, gs, out=out), steps=100, warmup=10,
+        t_call = med(lambda: rd.ragged_dot(lhs, rhs, gs, out=out), steps=100, warmup=10, per_call=True,
                      entry="tiny", prefix="call_")
         rd.ragged_dot(lhs, rhs, gs, out=out)
         torch.cuda.synchronize()
