@@ -932,9 +932,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         while (done < share) {
           const int64_t f = *fills;
-          const uint64_t target = (stages == 0 || f >= stages)
-                                      ? share
-                                      : share * static_cast<uint64_t>(f) / static_cast<uint64_t>(stages);
+          // dx (the fused GLU backward: zero rows twice as wide, a shorter GEMM)
+          // runs its zeros twice as fast as its stages, so that they are out
+          // before the CTA's last epilogues; the forward keeps them in step
+          constexpr uint64_t kLead = OP == kOpFwd ? 1 : 2;
+          uint64_t target = (stages == 0 || f >= stages)
+                                ? share
+                                : share * static_cast<uint64_t>(f) * kLead / static_cast<uint64_t>(stages);
+          if (target > share) target = share;
           if (target <= done) {
             // pacing only: give up (and unwind with the CTA) like any other wait
             if (*abort_flag) break;
