@@ -722,7 +722,7 @@ def run_rd(args):
              torch.empty((w.g_total,), dtype=torch.int32, device=device),
              torch.empty((w.m, w.n), dtype=torch.bfloat16, device=device)) for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    e2e_steps = max(3, min(args.steps, 10))
+    e2e_steps = max(3, min(args.steps, 20))
 
     def run_e2e(nsteps):
         loaded = [torch.cuda.Event() for _ in range(nsteps)]
