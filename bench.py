@@ -22,8 +22,9 @@ Also reported on the same line:
                 forward/backward, unsort backward, the fused GLU backward
                 through the down projection, the tiny workload's latency, and
                 the expert FFN forward graph from 256 to 16384 tokens), each as
-                time per call in us (calls back to back between two events,
-                the total divided by the calls, as for the headline), fraction
+                time per call in us (50 calls back to back between two events
+                after 10 warm-up calls, the total divided by the calls, as for
+                the headline), fraction
                 of its roofline and the bound ("t" tensor, "h" HBM, "l"
                 latency), with p10 / p90 of events around each call for the
                 five configs; short keys and 3-4 significant digits keep the
@@ -288,11 +289,13 @@ def run_ops(rd, device, stream, peaks):
         r["power_cap"] = "sw_power_cap" in c["reasons"]
         r["frac_sustained"] = flops / PS / (r["us"] * 1e-6)
 
-    def med(fn, steps=20, warmup=3, entry=None, prefix="", per_call=False):
+    def med(fn, steps=50, warmup=10, entry=None, prefix="", per_call=False):
         """Seconds per call: `steps` calls back to back between two events, divided by
         `steps` (as the headline's value), or with per_call the median of events around
         each call (a single call's latency); the p10 / p90 spread comes from the loop
-        with events around every call."""
+        with events around every call.  50 calls of these kernels last 5 to 25 ms, the
+        burst regime the burst peak is measured in (loops of 0.2 s and more run ~10 %
+        slower once the power cap acts)."""
         per, _ = time_launches(fn, steps, warmup, stream)
         if entry is not None:
             q = statistics.quantiles(per, n=10)
@@ -442,10 +445,10 @@ def run_ops(rd, device, stream, peaks):
             with torch.cuda.graph(g, stream=stream):
                 pair()
             tag = "decode_skewed" if skew else "decode_uniform"
-            t_pair = med(g.replay, steps=50, warmup=5, entry=tag, prefix="graph_pair_")
-            t_up = med(lambda: rd.ragged_dot(lhs, up, gs, epilogue=rd.EPI_SILU_GLU, out=h), 50, 5,
+            t_pair = med(g.replay, entry=tag, prefix="graph_pair_")
+            t_up = med(lambda: rd.ragged_dot(lhs, up, gs, epilogue=rd.EPI_SILU_GLU, out=h),
                        entry=tag, prefix="up_")
-            t_down = med(lambda: rd.ragged_dot(h, down, gs, out=o), 50, 5, entry=tag, prefix="down_")
+            t_down = med(lambda: rd.ragged_dot(h, down, gs, out=o), entry=tag, prefix="down_")
             live = int((w.group_sizes > 0).sum())
             B_up = w.m * w.k * 2 + live * w.k * w.n * 2 + w.m * (w.n // 2) * 2
             B_dn = w.m * (w.n // 2) * 2 + live * (w.n // 2) * w.k * 2 + w.m * w.k * 2
@@ -472,7 +475,7 @@ def run_ops(rd, device, stream, peaks):
         with torch.cuda.graph(g20, stream=stream):
             for _ in range(20):
                 rd.ragged_dot(lhs, rhs, gs, out=out)
-        t20 = med(g20.replay, steps=50, warmup=5)
+        t20 = med(g20.replay)
         res["tiny"] = {"us": t20 / 20 * 1e6, "call_us": t_call * 1e6, "bound": "latency",
                        "workload": w.name,
                        "note": "us: device time per launch (20 launches in one CUDA graph); "
@@ -952,7 +955,7 @@ def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["rd", "reference"], default="rd")
     ap.add_argument("--no-ops", action="store_true", help="skip the other hot-path rows")
     ap.add_argument("--no-cpu-baseline", action="store_true")
