@@ -18,6 +18,7 @@ Functions (same names as the C ABI, without the ``rd_`` prefix):
 * ``glu_bwd(fused, d_out, limit=None)``                  -> d_fused [rows, 2f]
 * ``unsort_bwd_rows(g, y, w, limit=None)``                -> (grad [rows, hidden], dot [rows])
 * ``set_tuning(...)``, ``get_tuning()``, ``tuning(...)``  -> the process-wide launch overrides
+* ``status_bits(status)``, ``check_status(status)``       -> read a status word (names, or raise)
 
 Every tensor of a call must sit on one CUDA device; the call runs on that
 device's current stream (or ``stream``).  A ``status`` word (a one-element
@@ -36,6 +37,7 @@ __all__ = [
     "glu_fwd", "glu_bwd", "unsort_bwd_rows", "RdError", "EPI_NONE", "EPI_SILU_GLU",
     "STATUS_NEG_SIZE", "STATUS_OVERFLOW", "STATUS_TIMEOUT", "MAX_GROUPS",
     "VARIANT_AUTO", "VARIANT_SINGLE", "VARIANT_PAIR", "set_tuning", "get_tuning", "tuning",
+    "status_bits", "check_status",
 ]
 
 EPI_NONE = 0
@@ -112,6 +114,29 @@ def _check(code: int, what: str):
     if code != 0:
         msg = _lib.rd_status_string(code).decode()
         raise RdError(code, f"{what}: {msg}")
+
+
+_STATUS_NAMES = ((STATUS_NEG_SIZE, "STATUS_NEG_SIZE: a group size < 0 was treated as 0"),
+                 (STATUS_OVERFLOW, "STATUS_OVERFLOW: the group sizes add up past m; boundaries clamped"),
+                 (STATUS_TIMEOUT, "STATUS_TIMEOUT: a bounded wait in a kernel ran out; outputs incomplete"))
+
+
+def status_bits(status) -> list:
+    """The names of the bits set in a status word (waits for the work queued before)."""
+    v = int(status.item())
+    return [name for bit, name in _STATUS_NAMES if v & bit]
+
+
+def check_status(status, allow=STATUS_NEG_SIZE | STATUS_OVERFLOW):
+    """Raise RdError if the status word holds a bit outside ``allow`` (by default only
+    STATUS_TIMEOUT raises: the size bits report data the kernels clamped and handled).
+    Reading the word waits for the calls that report into it."""
+    v = int(status.item())
+    bad = v & ~allow
+    if bad:
+        names = [name for bit, name in _STATUS_NAMES if bad & bit]
+        raise RdError(-1, "; ".join(names) or f"status bits {bad:#x}")
+    return v
 
 
 _torch_module = None

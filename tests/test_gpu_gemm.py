@@ -233,6 +233,11 @@ def test_status_bits(rd_lib):
     rd_lib.ragged_dot(lhs, rhs, _i32([100, -5, 200]), status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == (rd_lib.STATUS_NEG_SIZE | rd_lib.STATUS_OVERFLOW)
+    names = rd_lib.status_bits(status)
+    assert len(names) == 2 and names[0].startswith("STATUS_NEG_SIZE") and names[1].startswith("STATUS_OVERFLOW")
+    assert rd_lib.check_status(status) == 3            # the size bits alone do not raise
+    with pytest.raises(rd_lib.RdError, match="STATUS_NEG_SIZE"):
+        rd_lib.check_status(status, allow=0)
 
 
 # ------------------------------------------------------------------ tile-order bands

@@ -57,6 +57,8 @@ def test_timeout_unwinds_and_reports(rd_lib, variant, op):
         _call(rd_lib, op, a, w, do, gs, status)
     torch.cuda.synchronize()
     assert int(status.item()) & rd_lib.STATUS_TIMEOUT
+    with pytest.raises(rd_lib.RdError, match="STATUS_TIMEOUT"):
+        rd_lib.check_status(status)
     # the context, the tensor memory and the library are usable again
     status.zero_()
     with rd_lib.tuning(variant=v):
