@@ -585,6 +585,55 @@ def test_cuda_graph_follows_device_group_sizes(rd_lib):
         assert_close(_f64(h), ref, tol, f"graph replay sizes {sizes}")
 
 
+def test_cuda_graph_backward_follows_device_group_sizes(rd_lib):
+    """The backward of an expert FFN captured in one graph: the fused dx + GLU backward
+    through the down projection, dx of the up projection and both weight gradients (dw
+    with a preallocated workspace, so each replay rebuilds its per-group tensor maps on
+    the device); replays with new sizes equal the same calls made eagerly, bit for bit."""
+    rng = np.random.default_rng(11)
+    m, d, f, g = 1024, 256, 128, 5
+    x = _normal(rng, (m, d)).to(DEV)
+    up = _normal(rng, (g, d, 2 * f), 1 / d).to(DEV)
+    down = _normal(rng, (g, f, d), 1 / f).to(DEV)
+    fused = _normal(rng, (m, 2 * f), 4.0).to(DEV)
+    h = _normal(rng, (m, f)).to(DEV)
+    d_out = _normal(rng, (m, d)).to(DEV)
+    gs = _i32([200, 0, 300, 1, 500])
+    ws = torch.empty(rd_lib.dw_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    d_fused = torch.empty((m, 2 * f), dtype=torch.bfloat16, device=DEV)
+    dx = torch.empty((m, d), dtype=torch.bfloat16, device=DEV)
+    dw_down = torch.empty((g, f, d), dtype=torch.bfloat16, device=DEV)
+    dw_up = torch.empty((g, d, 2 * f), dtype=torch.bfloat16, device=DEV)
+
+    def step():
+        rd_lib.ragged_dot_trans_rhs_glu_bwd(d_out, down, fused, gs, out=d_fused)
+        rd_lib.ragged_dot_trans_rhs(d_fused, up, gs, out=dx)
+        rd_lib.trans_ragged_dot(h, d_out, gs, out=dw_down, workspace=ws)
+        rd_lib.trans_ragged_dot(x, d_fused, gs, out=dw_up, workspace=ws)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        step()                               # first calls outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step()
+    for sizes in ([200, 0, 300, 1, 500], [0, 1024, 0, 0, 0], [17, 333, 0, 601, 73]):
+        gs.copy_(_i32(sizes))
+        graph.replay()
+        torch.cuda.synchronize()
+        got = [t.clone() for t in (d_fused, dx, dw_down, dw_up)]
+        with torch.cuda.stream(s):
+            step()
+        torch.cuda.synchronize()
+        for a, b in zip(got, (d_fused, dx, dw_down, dw_up)):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"replay with sizes {sizes}"
+        # and the replayed dx of the up projection matches the oracle
+        ref = oracle.ragged_dot_trans_rhs(_f64(got[0].cpu()), _f64(up.cpu()), sizes)
+        tol = gemm_tol(ref, 2 * f, np.abs(_f64(got[0].cpu())).max(), np.abs(_f64(up.cpu())).max())
+        assert_close(_f64(got[1].cpu()), ref, tol, f"graph replay dx, sizes {sizes}")
+
+
 # ------------------------------------------------------------------ extremes
 def test_maximum_group_count(rd_lib):
     """g_total = RD_MAX_GROUPS (1024), most groups empty, an offset shard of 300 groups."""
