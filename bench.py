@@ -786,7 +786,10 @@ def run_rd(args):
         return (reps * h2d / (ti[0].elapsed_time(ti[1]) * 1e-3) / 1e9,
                 reps * d2h / (to[0].elapsed_time(to[1]) * 1e-3) / 1e9)
 
-    h2d_gbs, d2h_gbs = link_gbs()
+    # the best of three short measurements: the host link is shared with the rest of the
+    # machine, and one slow moment would otherwise set the bound
+    trials = [link_gbs() for _ in range(3)]
+    h2d_gbs, d2h_gbs = max(t[0] for t in trials), max(t[1] for t in trials)
     step_floor_s = max(h2d / (h2d_gbs * 1e9), d2h / (d2h_gbs * 1e9), ms_per_step * 1e-3)
     e2e_limit = world * flops / step_floor_s / 1e12
     del bufs
