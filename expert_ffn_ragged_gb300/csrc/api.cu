@@ -17,7 +17,7 @@ namespace rd {
 namespace {
 
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // default bound of any single wait in a kernel
-constexpr int32_t kBandRows = 4096;              // default rows per band of the fwd/dx tile order
+constexpr int32_t kBandRows = 6144;              // default rows per band of the fwd/dx tile order
 
 // Process-wide tuning overrides (rd_set_tuning); 0 = the default.
 std::atomic<int32_t> g_variant{RD_VARIANT_AUTO};

@@ -16,7 +16,7 @@
 //     boundaries (exclusive prefix clamped to L) and the per-group tile
 //     prefix in shared memory -- no workspace, no host round trip;
 //   * tiles are handed out by static striding over (group, band, n-tile,
-//     m-tile): within a band of rows (4096 by default) the m-tiles run
+//     m-tile): within a band of rows (6144 by default) the m-tiles run
 //     fastest, so the CTAs working at one time share each rhs column panel
 //     through L2 and the band's lhs rows stay in L2 until every column panel
 //     has used them;

@@ -314,7 +314,7 @@ rd_status rd_unsort_bwd_rows(const void* g, const void* y, const float* w, void*
  *   band_rows        rows per band of the forward / dx tile order (within a
  *                    band the CTAs sweep every output column block before the
  *                    next band starts, so the band's lhs rows stay in L2);
- *                    0 = the default, 4096.  Rounded down to whole tiles
+ *                    0 = the default, 6144.  Rounded down to whole tiles
  *                    (at least one).
  *   wait_timeout_ns  bound of every wait inside the grouped-GEMM kernels;
  *                    0 = the default, 4 s.

@@ -243,7 +243,7 @@ def test_status_bits(rd_lib):
 # ------------------------------------------------------------------ tile-order bands
 # The forward / dx tile order walks each group in bands of band_tiles m-tiles
 # (the last band of a group partial), sweeping every column block inside a
-# band.  With the default 4096-row band only groups above 4096 rows span
+# band.  With the default 6144-row band only groups above 6144 rows span
 # several bands, so these tests shrink the band to 1, 2 and 3 tiles: groups of
 # 600 to 2000 rows then hold up to 16 bands, most of them with a partial last
 # band, over several column tiles, and every output element is compared.
